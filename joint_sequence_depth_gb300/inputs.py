@@ -1,0 +1,84 @@
+"""Seeded synthetic inputs for MoDA, shared by the tests, the smoke check and the benchmark.
+
+This module holds no MoDA arithmetic: it only names the workload shapes and
+draws i.i.d. N(0, 1) tensors from a seeded ``torch.Generator``, in a fixed
+order (q, k, v, kd, vd, then dout), in float32, then rounds them to the storage
+type (bf16 round-to-nearest-even).  The kernel benchmark on the MoDA page
+(Table 2 / Table 7) times random tensors, so these synthetic inputs are the
+workload itself, not a stand-in for a dataset.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Shape:
+    """One MoDA problem: B batch, H query heads, Hkv kv heads, T tokens, d head dim,
+    S depth slots per position (the depth slots of the layer's history H_l)."""
+
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    T: int
+    d: int
+    S: int
+    dtype: torch.dtype
+    backward: bool = False
+
+    @property
+    def G(self) -> int:
+        return self.H // self.Hkv
+
+
+# The workloads MoDA is measured and checked on.
+WORKLOADS = {
+    "fp32_small": Shape("fp32_small", 1, 2, 2, 256, 64, 4, torch.float32),
+    "bf16_mha": Shape("bf16_mha", 2, 16, 16, 2048, 128, 8, torch.bfloat16),
+    "bf16_gqa": Shape("bf16_gqa", 4, 32, 8, 4096, 128, 24, torch.bfloat16),
+    "bf16_long": Shape("bf16_long", 1, 32, 8, 16384, 128, 48, torch.bfloat16),
+    "bf16_train": Shape("bf16_train", 8, 16, 4, 4096, 64, 32, torch.bfloat16, backward=True),
+}
+
+# seed of each workload (its index in the list above, from 1)
+SEEDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
+
+
+def make_inputs(shape: Shape, seed: int, device="cpu", with_dout: bool | None = None, dtype=None):
+    """Draw q, k, v, kd, vd (and dout when requested) for ``shape``.
+
+    Layouts: q/dout [B,H,T,d]; k/v [B,Hkv,T,d]; kd/vd [B,Hkv,T,S,d]; all dense
+    row-major.  The generator lives on ``device`` (CPU and CUDA streams differ,
+    so a given use always draws on the same device).
+    """
+    dtype = dtype or shape.dtype
+    if with_dout is None:
+        with_dout = shape.backward
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    B, H, Hkv, T, d, S = shape.B, shape.H, shape.Hkv, shape.T, shape.d, shape.S
+    dims = {
+        "q": (B, H, T, d),
+        "k": (B, Hkv, T, d),
+        "v": (B, Hkv, T, d),
+        "kd": (B, Hkv, T, S, d),
+        "vd": (B, Hkv, T, S, d),
+    }
+    if with_dout:
+        dims["dout"] = (B, H, T, d)
+    out = {}
+    for key, shp in dims.items():
+        x = torch.randn(shp, generator=gen, device=device, dtype=torch.float32)
+        out[key] = x if dtype == torch.float32 else x.to(dtype)
+        del x
+    return out
+
+
+def scaled(shape: Shape, **changes) -> Shape:
+    """A copy of ``shape`` with some sizes changed (for small parity cases)."""
+    fields = dict(shape.__dict__)
+    fields.update(changes)
+    return Shape(**fields)
