@@ -1,0 +1,114 @@
+/*
+ * moda.h — C ABI of the MoDA (Mixture-of-Depths Attention) library for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation (paper "Mixture-of-Depths Attention", arXiv:2603.15619; slides frame
+ * "One denominator allocates probability across both memories", teaching form of
+ * Sec. 2.2 and Algorithm 1): for batch b, query head h, position t, with
+ * kv head g = h / G and G = H / Hkv (consecutive query heads share a kv head,
+ * G = H_q / H_k as in the slides' Table 1 frame):
+ *
+ *     a_j = scale * q[b,h,t,:] . k[b,g,j,:]            j = 0 .. t     (causal)
+ *     b_i = scale * q[b,h,t,:] . kd[b,g,t,i,:]         i = 0 .. S-1   (same position)
+ *     o[b,h,t,:] = (sum_j e^{a_j} v[b,g,j,:] + sum_i e^{b_i} vd[b,g,t,i,:])
+ *                  / (sum_j e^{a_j} + sum_i e^{b_i})
+ *     lse[b,h,t] = ln(sum_j e^{a_j} + sum_i e^{b_i})
+ *
+ * Both memories share ONE softmax denominator; the depth slots are never
+ * normalised separately (same frame, and "Shared online-softmax states
+ * preserve the joint operator", Algorithm 1).  S = 0 is plain causal attention.
+ *
+ * Layouts: every tensor is dense, contiguous and row-major exactly as shaped:
+ *     q, o, dout, dq        [B, H,   T, d]
+ *     k, v, dk, dv          [B, Hkv, T, d]
+ *     kd, vd, dkd, dvd      [B, Hkv, T, S, d]   (the [S, d] slab of one position is contiguous)
+ *     lse                   [B, H,   T]         float32, natural log
+ * Element type: all of q..vd, o, dout and the gradients share desc->dtype;
+ * lse is always float32.  Arithmetic accumulates in float32.
+ *
+ * Ownership: the caller owns every buffer (device memory unless a function says
+ * otherwise); the library keeps no pointer after a call returns and allocates no
+ * device memory.  Every device pointer must be 16-byte aligned.
+ *
+ * Streams: work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and the call returns without waiting, unless MODA_SYNC=1 is set in the
+ * environment, in which case each call waits for its stream and reports device-side
+ * errors (see moda_device_status).
+ *
+ * Errors: invalid or unsupported arguments are reported synchronously and
+ * nothing is launched.  A failed launch returns MODA_ERR_CUDA.  Kernels never
+ * trap: a bounded wait that runs out records MODA_ERR_TIMEOUT in a device status
+ * word and the kernel returns early (its outputs are then undefined).
+ */
+#ifndef MODA_H_
+#define MODA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MODA_OK = 0,
+  MODA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, H % Hkv != 0 */
+  MODA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, dtype) */
+  MODA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MODA_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
+  MODA_ERR_WORKSPACE = 5     /* workspace missing or smaller than moda_bwd_workspace_bytes */
+} moda_status;
+
+typedef enum { MODA_DTYPE_F32 = 0, MODA_DTYPE_BF16 = 1 } moda_dtype;
+
+/* Problem description.  B >= 1, H >= 1, Hkv >= 1 with H % Hkv == 0, T >= 1,
+ * S >= 0 (S = 0: the depth history H_l is empty), d in {64, 128}.
+ * scale <= 0 selects 1/sqrt(d) (the slides' a_j, b_i use 1/sqrt(d)). */
+typedef struct {
+  int32_t B, H, Hkv, T, S, d;
+  int32_t dtype; /* moda_dtype */
+  float scale;
+} moda_desc;
+
+/* Forward (the operation above).
+ * In:  q, k, v, kd, vd (device, desc->dtype; kd/vd may be NULL when S == 0).
+ * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it).
+ * bf16 runs on the tensor cores (tcgen05, float32 accumulation, P rounded to
+ * bf16 for the PV product); float32 runs on the CUDA cores in float32. */
+moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, void* o, float* lse, void* stream);
+
+/* Bytes of device workspace moda_bwd needs for `desc` (float32 row statistics
+ * and the float32 dq accumulator).  0 on invalid desc. */
+size_t moda_bwd_workspace_bytes(const moda_desc* desc);
+
+/* Backward: gradients of L = sum(dout * o) for the forward above (the pages give
+ * no backward; this is the analytic gradient of the operation).  With
+ * P = exp(score - lse), D_t = sum(dout_t * o_t), dS = P * (dout . value - D_t):
+ *     dq  = scale * sum dS * key            (sequence keys and depth slots)
+ *     dk  = scale * sum dS * q,  dv  = sum P * dout   (summed over the G heads and rows t >= j)
+ *     dkd = scale * sum dS * q,  dvd = sum P * dout   (summed over the G heads of position t)
+ * In:  q, k, v, kd, vd, o, lse (as written by moda_fwd), dout (device).
+ * Out: dq, dk, dv, dkd, dvd (device, desc->dtype; dkd/dvd may be NULL when S == 0).
+ * workspace: device scratch of at least moda_bwd_workspace_bytes(desc) bytes,
+ * 256-byte aligned; its contents on entry do not matter.  Calls that share a
+ * workspace must not overlap on the GPU. */
+moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                     void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reads the device status word that bounded waits write (MODA_OK when clean) and,
+ * when `clear` is non-zero, resets it.  Waits for `stream` first. */
+moda_status moda_device_status(int clear, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* moda_status_str(moda_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t moda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MODA_H_ */

@@ -1,0 +1,147 @@
+"""Python binding of the MoDA C ABI (include/moda.h): argument marshalling only.
+
+Each function takes torch CUDA tensors, allocates missing outputs with torch
+(device memory is torch's), and hands raw pointers to ``libmoda.so``.  Every
+step of the computation runs in the library's CUDA kernels; if the library is
+missing this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+MODA_OK = 0
+STATUS_NAMES = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTED", 3: "MODA_ERR_CUDA",
+                4: "MODA_ERR_TIMEOUT", 5: "MODA_ERR_WORKSPACE"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+# Names of every function include/moda.h declares.
+EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status", "moda_status_str",
+           "moda_version")
+
+
+class MODAError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class moda_desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("T", ctypes.c_int32),
+                ("S", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Loads libmoda.so (built in-tree by ``build.build()``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libmoda.so is not built ({_build.LIB}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(_build.LIB)
+            p, d = ctypes.c_void_p, ctypes.POINTER(moda_desc)
+            lib.moda_fwd.argtypes = [d, p, p, p, p, p, p, p, p]
+            lib.moda_fwd.restype = ctypes.c_int
+            lib.moda_bwd_workspace_bytes.argtypes = [d]
+            lib.moda_bwd_workspace_bytes.restype = ctypes.c_size_t
+            lib.moda_bwd.argtypes = [d] + [p] * 14 + [ctypes.c_size_t, p]
+            lib.moda_bwd.restype = ctypes.c_int
+            lib.moda_device_status.argtypes = [ctypes.c_int, p]
+            lib.moda_device_status.restype = ctypes.c_int
+            lib.moda_status_str.argtypes = [ctypes.c_int]
+            lib.moda_status_str.restype = ctypes.c_char_p
+            lib.moda_version.argtypes = []
+            lib.moda_version.restype = ctypes.c_int32
+            _lib = lib
+    return _lib
+
+
+def make_desc(B, H, Hkv, T, S, d, dtype, scale=None) -> moda_desc:
+    return moda_desc(B, H, Hkv, T, S, d, DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype),
+                     float(scale or 0.0))
+
+
+def _desc_from(q, k, kd, scale):
+    B, H, T, d = q.shape
+    Hkv = k.shape[1]
+    S = kd.shape[3] if kd is not None else 0
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    return make_desc(B, H, Hkv, T, S, d, q.dtype, scale)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_like(t, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None):
+    """Joint sequence/depth attention forward.  Returns (o [B,H,T,d], lse [B,H,T] float32)."""
+    desc = _desc_from(q, k, kd, scale)
+    B, H, T, d = q.shape
+    for t, name in ((k, "k"), (v, "v")):
+        _check_like(t, q.dtype, (B, desc.Hkv, T, d), name)
+    if desc.S:
+        for t, name in ((kd, "kd"), (vd, "vd")):
+            _check_like(t, q.dtype, (B, desc.Hkv, T, desc.S, d), name)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    st = load_library().moda_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None,
+                                 _ptr(vd) if desc.S else None, _ptr(o), _ptr(lse), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_fwd")
+    return o, lse
+
+
+def moda_bwd_workspace_bytes(desc: moda_desc) -> int:
+    return int(load_library().moda_bwd_workspace_bytes(ctypes.byref(desc)))
+
+
+def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=None, stream=None):
+    """Backward of moda_fwd.  Returns (dq, dk, dv, dkd, dvd) in the input dtype."""
+    desc = _desc_from(q, k, kd, scale)
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty_like(kd) if desc.S else None, torch.empty_like(vd) if desc.S else None)
+    dq, dk, dv, dkd, dvd = grads
+    need = moda_bwd_workspace_bytes(desc)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load_library().moda_bwd(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None, _ptr(vd) if desc.S else None,
+        _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkd) if desc.S else None,
+        _ptr(dvd) if desc.S else None, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_bwd")
+    return dq, dk, dv, dkd, dvd
+
+
+def moda_device_status(clear=True, stream=None) -> int:
+    return int(load_library().moda_device_status(1 if clear else 0, _stream(stream)))

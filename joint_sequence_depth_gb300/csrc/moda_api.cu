@@ -1,0 +1,189 @@
+// C ABI of the MoDA library (declared in include/moda.h): argument checks,
+// kernel selection and launches.  All compute runs in the kernels of this
+// directory; nothing here touches tensor data on the host.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "moda.h"
+#include "moda_common.cuh"
+
+namespace {
+
+// Device status word that bounded waits write (MODA_ERR_TIMEOUT) instead of trapping.
+__device__ int g_status_word = 0;
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t mul_capped(int64_t a, int64_t b) {
+  if (a <= 0 || b <= 0) return a * b;
+  if (a > kMaxElems / b) return kMaxElems + 1;
+  return a * b;
+}
+
+moda_status check_desc(const moda_desc* d) {
+  if (d == nullptr) return MODA_ERR_INVALID_ARG;
+  if (d->B < 1 || d->H < 1 || d->Hkv < 1 || d->T < 1 || d->S < 0 || d->d < 1) return MODA_ERR_INVALID_ARG;
+  if (d->H % d->Hkv != 0) return MODA_ERR_INVALID_ARG;
+  if (!(d->scale <= 0.f || std::isfinite(d->scale))) return MODA_ERR_INVALID_ARG;
+  if (d->dtype != MODA_DTYPE_F32 && d->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
+  if (d->d != 64 && d->d != 128) return MODA_ERR_UNSUPPORTED;
+  const int64_t q = mul_capped(mul_capped(mul_capped(d->B, d->H), d->T), d->d);
+  const int64_t kd = mul_capped(mul_capped(mul_capped(mul_capped(d->B, d->Hkv), d->T), d->S), d->d);
+  if (q > kMaxElems || kd > kMaxElems) return MODA_ERR_INVALID_ARG;
+  return MODA_OK;
+}
+
+moda::Problem problem_of(const moda_desc* d) {
+  moda::Problem p;
+  p.B = d->B;
+  p.H = d->H;
+  p.Hkv = d->Hkv;
+  p.T = d->T;
+  p.S = d->S;
+  p.d = d->d;
+  p.G = d->H / d->Hkv;
+  p.scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->d));
+  p.scale_log2 = p.scale * moda::kLog2e;
+  return p;
+}
+
+bool sync_mode() {
+  const char* e = std::getenv("MODA_SYNC");
+  return e != nullptr && e[0] == '1';
+}
+
+int* status_word() {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(ptr);
+}
+
+moda_status read_status(int clear, cudaStream_t s) {
+  int* w = status_word();
+  if (w == nullptr) return MODA_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, w, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MODA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MODA_ERR_CUDA;
+  if (clear && host != 0) {
+    if (cudaMemsetAsync(w, 0, sizeof(int), s) != cudaSuccess) return MODA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MODA_ERR_CUDA;
+  }
+  return static_cast<moda_status>(host);
+}
+
+moda_status finish(cudaError_t launch, cudaStream_t s) {
+  if (launch != cudaSuccess) return MODA_ERR_CUDA;
+  if (sync_mode()) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MODA_ERR_CUDA;
+    return read_status(1, s);
+  }
+  return MODA_OK;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t delta_bytes(const moda_desc* d) { return align256(size_t(d->B) * d->H * d->T * sizeof(float)); }
+size_t dq_accum_bytes(const moda_desc* d) {
+  return align256(size_t(d->B) * d->H * d->T * d->d * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" {
+
+moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, void* o, float* lse, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (!q || !k || !v || !o) return MODA_ERR_INVALID_ARG;
+  if (desc->S > 0 && (!kd || !vd)) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, kd, vd, static_cast<const void*>(o), static_cast<const void*>(lse)})
+    if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
+  moda::FwdArgs a;
+  a.p = problem_of(desc);
+  a.status = status_word();
+  if (a.status == nullptr) return MODA_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.kd = desc->S > 0 ? kd : nullptr;
+  a.vd = desc->S > 0 ? vd : nullptr;
+  a.o = o;
+  a.lse = lse;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (desc->dtype == MODA_DTYPE_BF16 && moda::fwd_sm103_supported(a.p))
+    e = moda::launch_fwd_sm103(a, s);
+  else
+    e = moda::launch_fwd_simt(a, desc->dtype, s);
+  return finish(e, s);
+}
+
+size_t moda_bwd_workspace_bytes(const moda_desc* desc) {
+  if (check_desc(desc) != MODA_OK) return 0;
+  return delta_bytes(desc) + dq_accum_bytes(desc);
+}
+
+moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                     void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return MODA_ERR_INVALID_ARG;
+  if (desc->S > 0 && (!kd || !vd || !dkd || !dvd)) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, kd, vd, o, static_cast<const void*>(lse), dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv), static_cast<const void*>(dkd),
+                        static_cast<const void*>(dvd)})
+    if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < moda_bwd_workspace_bytes(desc)) return MODA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MODA_ERR_INVALID_ARG;
+  moda::BwdArgs a;
+  a.p = problem_of(desc);
+  a.status = status_word();
+  if (a.status == nullptr) return MODA_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.kd = desc->S > 0 ? kd : nullptr;
+  a.vd = desc->S > 0 ? vd : nullptr;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dkd = desc->S > 0 ? dkd : nullptr;
+  a.dvd = desc->S > 0 ? dvd : nullptr;
+  a.delta = static_cast<float*>(workspace);
+  a.dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(desc));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (desc->dtype == MODA_DTYPE_BF16 && moda::bwd_sm103_supported(a.p))
+    e = moda::launch_bwd_sm103(a, s);
+  else
+    e = moda::launch_bwd_simt(a, desc->dtype, s);
+  return finish(e, s);
+}
+
+moda_status moda_device_status(int clear, void* stream) {
+  return read_status(clear, static_cast<cudaStream_t>(stream));
+}
+
+const char* moda_status_str(moda_status status) {
+  switch (status) {
+    case MODA_OK: return "MODA_OK";
+    case MODA_ERR_INVALID_ARG: return "MODA_ERR_INVALID_ARG";
+    case MODA_ERR_UNSUPPORTED: return "MODA_ERR_UNSUPPORTED";
+    case MODA_ERR_CUDA: return "MODA_ERR_CUDA";
+    case MODA_ERR_TIMEOUT: return "MODA_ERR_TIMEOUT";
+    case MODA_ERR_WORKSPACE: return "MODA_ERR_WORKSPACE";
+  }
+  return "MODA_ERR_UNKNOWN";
+}
+
+int32_t moda_version(void) { return 100; }
+
+}  // extern "C"

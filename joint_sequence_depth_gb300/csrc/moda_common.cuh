@@ -1,0 +1,64 @@
+// Shared definitions of the MoDA CUDA library (kernels and host dispatch).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moda {
+
+// log2(e): the slides' Algorithm 1 uses 2^(S-m); folding log2(e) into the score
+// scale makes that the natural-exponential softmax of the operation
+// (frame "Backup: pseudocode needs implementation-level checks").
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status word codes (mirror moda_status).
+constexpr int kStatusTimeout = 4;
+
+struct Problem {
+  int B, H, Hkv, T, S, d, G;
+  float scale;       // score scale (1/sqrt(d) by default)
+  float scale_log2;  // scale * log2(e)
+};
+
+struct FwdArgs {
+  Problem p;
+  int* status;  // device status word (bounded-wait timeouts)
+  const void *q, *k, *v, *kd, *vd;
+  void* o;
+  float* lse;  // may be null
+};
+
+struct BwdArgs {
+  Problem p;
+  int* status;
+  const void *q, *k, *v, *kd, *vd, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv, *dkd, *dvd;
+  float* delta;     // workspace [B,H,T]: D_t = dout_t . o_t
+  float* dq_accum;  // workspace [B,H,T,d] float32 (tensor-core path)
+};
+
+// Element loads/stores for the two storage types.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Records the first error code in the device status word (never traps).
+__device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Host-side launchers (one per kernel family).  Each returns the launch error.
+cudaError_t launch_fwd_simt(const FwdArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s);
+bool fwd_sm103_supported(const Problem& p);
+bool bwd_sm103_supported(const Problem& p);
+
+}  // namespace moda

@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/moda.h declares,
+and rejects bad arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from joint_sequence_depth_gb300 import binding
+from joint_sequence_depth_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moda_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(binding.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert lib.moda_status_str(code).decode() == name
+    assert lib.moda_version() >= 100
+
+
+def desc(**kw):
+    base = dict(B=1, H=4, Hkv=2, T=16, S=3, d=64, dtype=1, scale=0.0)
+    base.update(kw)
+    return binding.moda_desc(base["B"], base["H"], base["Hkv"], base["T"], base["S"], base["d"], base["dtype"],
+                             base["scale"])
+
+
+FAKE = 1 << 20  # aligned fake device address: validation must fail before any use
+
+
+def fwd(lib, d, ptrs=None):
+    p = [ctypes.c_void_p(FAKE)] * 7 if ptrs is None else ptrs
+    return lib.moda_fwd(ctypes.byref(d) if d is not None else None, *p, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=3, Hkv=2), 1), (dict(T=0), 1), (dict(B=0), 1), (dict(S=-1), 1), (dict(Hkv=0), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(dtype=7), 2), (dict(scale=float("nan")), 1),
+])
+def test_forward_rejects_bad_desc(lib, kw, status):
+    assert fwd(lib, desc(**kw)) == status
+
+
+def test_forward_rejects_null_and_misaligned(lib):
+    assert fwd(lib, None) == 1
+    ptrs = [ctypes.c_void_p(FAKE)] * 7
+    for i in (0, 1, 2, 5):
+        bad = list(ptrs)
+        bad[i] = None
+        assert fwd(lib, desc(), bad) == 1
+    for i in range(7):
+        bad = list(ptrs)
+        bad[i] = ctypes.c_void_p(FAKE + 8)
+        assert fwd(lib, desc(), bad) == 1
+    # depth pointers may be null only when S == 0
+    bad = list(ptrs)
+    bad[3] = None
+    assert fwd(lib, desc(S=3), bad) == 1
+
+
+def test_backward_workspace_contract(lib):
+    d = desc(B=2, H=4, Hkv=2, T=100, S=3, d=64)
+    need = lib.moda_bwd_workspace_bytes(ctypes.byref(d))
+    assert need >= 2 * 4 * 100 * 4 + 2 * 4 * 100 * 64 * 4
+    assert lib.moda_bwd_workspace_bytes(ctypes.byref(desc(H=3))) == 0
+    ptrs = [ctypes.c_void_p(FAKE)] * 13
+    ws = ctypes.c_void_p(FAKE)
+    # too small / missing workspace
+    assert lib.moda_bwd(ctypes.byref(d), *ptrs, ws, ctypes.c_size_t(need - 1), None) == 5
+    assert lib.moda_bwd(ctypes.byref(d), *ptrs, None, ctypes.c_size_t(need), None) == 5
+    # workspace not 256-byte aligned
+    assert lib.moda_bwd(ctypes.byref(d), *ptrs, ctypes.c_void_p(FAKE + 16), ctypes.c_size_t(need), None) == 1
