@@ -14,7 +14,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Device status word codes (mirror moda_status).
-constexpr int kStatusTimeout = 4;
+constexpr int kStatusConfig = 3;   // a kernel refused its launch configuration (MODA_ERR_CUDA)
+constexpr int kStatusTimeout = 4;  // a bounded wait ran out (MODA_ERR_TIMEOUT)
 
 struct Problem {
   int B, H, Hkv, T, S, d, G;

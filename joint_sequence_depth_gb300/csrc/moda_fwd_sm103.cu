@@ -55,34 +55,34 @@ constexpr int BN = 128;                    // keys per K/V tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kDepthWarps = 4;
 constexpr int kDepthStages = 2;
-constexpr int kDepthStageBytes = 9216;
+constexpr int kSmemLimit = 232448;  // bytes of dynamic shared memory a CTA may use
 
-template <int D, int SC>
+// Shared memory: Q tile | K/V ring (NSLOT tiles) | depth rings (4 warps x 2 stages of
+// `dstage` bytes, sized on the host) | barriers | misc.  With NSLOT >= 4 the load of
+// K_{j+2} only waits for K_j's slot, so it is in flight while PV_j runs.
+template <int D, int SC, int NSLOT_>
 struct FwdCfg {
+  static constexpr int NSLOT = NSLOT_;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int NSLOT = D == 128 ? 3 : 6;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int SUB = SC * D * 2;   // one position's sub-slab of SC slots
   static constexpr int STRIDE = SUB + 16;  // staggered position stride in a stage
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + Q_BYTES;
   static constexpr int OFF_DEP = OFF_KV + NSLOT * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_DEP + kDepthWarps * kDepthStages * kDepthStageBytes;
   // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[2], p_full[2], pv_done[2], depth_done, drain,
   // dfull[4*NB], dempty[4*NB]
   static constexpr int NBAR = 2 * NSLOT + 9 + 2 * kDepthWarps * kDepthStages;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_MD = OFF_MISC + 16;
-  static constexpr int OFF_LD = OFF_MD + BM * 4;
-  static constexpr int SMEM_USED = OFF_LD + BM * 4;
-  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  static constexpr int TAIL = NBAR * 8 + 16 + 2 * BM * 4;  // barriers, misc words, m_d[], l_d[]
   static constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_OD = 256 + D;
   static constexpr uint32_t TM_COLS = 512;
-  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static constexpr int off_bar(int dstage) { return OFF_DEP + kDepthWarps * kDepthStages * dstage; }
+  static constexpr int smem_alloc(int dstage) { return off_bar(dstage) + TAIL; }
 };
 
 struct FwdTcParams {
   int B, H, Hkv, T, S, G, P, n_pb;
+  int dstage;  // bytes of one depth ring stage (multiple of 16)
   float scale_log2;
   const __nv_bfloat16* q;
   const __nv_bfloat16* kd;
@@ -103,14 +103,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, int SC>
+template <int D, int SC, int NSLOT>
 __global__ void __launch_bounds__(384, 1)
     moda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const FwdTcParams p) {
-  using C = FwdCfg<D, SC>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using C = FwdCfg<D, SC, NSLOT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  // The 128-byte swizzle atoms need 1024-byte aligned tiles; the dynamic shared window
+  // starts 1024-aligned on this architecture, and a launch where it does not is refused.
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kStatusConfig);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = p.B * p.Hkv;
@@ -122,7 +127,8 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = p_last / BN + 1;
   const int n_dchunks = (p.S + SC - 1) / SC;  // depth slot groups (each: K pass then V pass)
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const int off_bar = C::off_bar(p.dstage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off_bar);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + C::NSLOT;
   uint64_t* q_full = bars + 2 * C::NSLOT;
@@ -133,10 +139,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* drain = depth_done + 1;
   uint64_t* dfull = drain + 1;
   uint64_t* dempty = dfull + kDepthWarps * kDepthStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* md_s = reinterpret_cast<float*>(smem + C::OFF_MD);
-  float* ld_s = reinterpret_cast<float*>(smem + C::OFF_LD);
+  uint8_t* misc = smem + off_bar + C::NBAR * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  float* md_s = reinterpret_cast<float*>(misc + 16);
+  float* ld_s = md_s + BM;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSLOT; ++i) {
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(384, 1)
         if (lane < nvalid) {
           const int k = kw0 + lane;
           const __nv_bfloat16* src = src_base + ((static_cast<int64_t>(bg) * p.T + p0 + k) * p.S + i0) * D;
-          const uint32_t dst = sbase + C::OFF_DEP + bi * kDepthStageBytes + lane * C::STRIDE;
+          const uint32_t dst = sbase + C::OFF_DEP + bi * p.dstage + lane * C::STRIDE;
           bulk_load(dst, src, bytes, &dfull[bi]);
         }
       }
@@ -308,20 +315,23 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
       const int kb = j * BN;
-      float mx = -INFINITY;
       if (kb + BN - 1 > p0 || !valid) {
+        // diagonal tile (or dead row): keys after the row's position are invisible
+        const int lim = valid ? pos - kb : -1;
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const bool vis = valid && (kb + c <= pos);
-          const float v = vis ? __uint_as_float(s[c]) : -INFINITY;
-          s[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int c = 0; c < BN; ++c)
+          if (c > lim) s[c] = __float_as_uint(-INFINITY);
       }
-      const float m_tile = mx * sl2;
+      // row max: four independent chains of 3-input max
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; c += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+      }
+      const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
       if (j == 0) {
         m_run = m_tile;
       } else {
@@ -346,16 +356,26 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
+      // p = 2^(s*scale*log2e - m): packed FMA, MUFU ex2, packed row-sum in four chains
+      float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float e0 = ex2(fmaf(__uint_as_float(s[c]), sl2, -m_use));
-        const float e1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -m_use));
-        lsum += e0 + e1;
-        pk[c >> 1] = pack_bf16(e0, e1);
+      for (int c = 0; c < BN; c += 4) {
+        float x0, x1, x2, x3;
+        ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
+        ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
+        x0 = ex2(x0);
+        x1 = ex2(x1);
+        x2 = ex2(x2);
+        x3 = ex2(x3);
+        if ((c & 4) == 0)
+          fadd2(ls0, ls1, x0, x1), fadd2(ls0, ls1, x2, x3);
+        else
+          fadd2(ls2, ls3, x0, x1), fadd2(ls2, ls3, x2, x3);
+        pk[c >> 1] = pack_bf16(x0, x1);
+        pk[(c >> 1) + 1] = pack_bf16(x2, x3);
       }
-      l_run += lsum;
+      l_run += (ls0 + ls1) + (ls2 + ls3);
       // P_j (bf16 pairs) into the first 64 columns of S_j's TMEM buffer
       tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -442,27 +462,33 @@ __global__ void __launch_bounds__(384, 1)
       int bi = w * kDepthStages + c % kDepthStages;
       ok = warp_wait(&dfull[bi], (c / kDepthStages) & 1, abort_flag);
       if (!ok) break;
-      float sc[SC];
+      // two partial sums per slot (even / odd 16-byte chunks) for instruction-level parallelism
+      float sc[SC], sc2[SC];
 #pragma unroll
-      for (int i = 0; i < SC; ++i) sc[i] = 0.f;
+      for (int i = 0; i < SC; ++i) sc[i] = sc2[i] = 0.f;
       if (valid) {
-        const uint32_t kbuf = sbase + C::OFF_DEP + bi * kDepthStageBytes + kl * C::STRIDE;
+        const uint32_t kbuf = sbase + C::OFF_DEP + bi * p.dstage + kl * C::STRIDE;
 #pragma unroll
         for (int ch = 0; ch < D / 8; ++ch) {
 #pragma unroll
           for (int i = 0; i < SC; ++i) {
             if (i < nc) {
               const uint4 kv = ld_shared_v4(kbuf + i * (D * 2) + ch * 16);
-              float a = sc[i];
+              float a = (ch & 1) ? sc2[i] : sc[i];
               a = dot2_bf16(qv[ch].x, kv.x, a);
               a = dot2_bf16(qv[ch].y, kv.y, a);
               a = dot2_bf16(qv[ch].z, kv.z, a);
               a = dot2_bf16(qv[ch].w, kv.w, a);
-              sc[i] = a;
+              if (ch & 1)
+                sc2[i] = a;
+              else
+                sc[i] = a;
             }
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < SC; ++i) sc[i] += sc2[i];
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[bi]);
       // ---- online update of (m_d, l_d) with this slot group
@@ -487,7 +513,7 @@ __global__ void __launch_bounds__(384, 1)
       bi = w * kDepthStages + c % kDepthStages;
       ok = warp_wait(&dfull[bi], (c / kDepthStages) & 1, abort_flag);
       if (!ok) break;
-      const uint32_t vbuf = sbase + C::OFF_DEP + bi * kDepthStageBytes + kl * C::STRIDE;
+      const uint32_t vbuf = sbase + C::OFF_DEP + bi * p.dstage + kl * C::STRIDE;
 #pragma unroll 1
       for (int g32 = 0; g32 < D / 32; ++g32) {
         uint32_t acc[32];
@@ -577,18 +603,29 @@ int positions_per_warp(int G, int P) {
   return most;
 }
 
-template <int D, int SC>
-cudaError_t launch_cfg(const FwdTcParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-  using C = FwdCfg<D, SC>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(moda_fwd_tc_kernel<D, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
+// Depth stage bytes for slot groups of SC: the staggered sub-slabs of the most positions
+// one depth warp covers.
+int depth_stage_bytes(int npos, int sc, int D) { return npos * (sc * D * 2 + 16); }
+
+template <int D, int SC, int NSLOT>
+bool fits(int npos) {
+  return FwdCfg<D, SC, NSLOT>::smem_alloc(depth_stage_bytes(npos, SC, D)) <= kSmemLimit;
+}
+
+template <int D, int SC, int NSLOT>
+cudaError_t launch_cfg(FwdTcParams p, int npos, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  using C = FwdCfg<D, SC, NSLOT>;
+  p.dstage = depth_stage_bytes(npos, SC, D);
+  const int smem = C::smem_alloc(p.dstage);
+  static int attr_bytes = 0;
+  if (attr_bytes < smem) {
+    cudaError_t e =
+        cudaFuncSetAttribute(moda_fwd_tc_kernel<D, SC, NSLOT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_bytes = smem;
   }
   const unsigned grid = static_cast<unsigned>(p.n_pb) * p.B * p.Hkv;
-  moda_fwd_tc_kernel<D, SC><<<grid, 384, C::SMEM_ALLOC, s>>>(tk, tv, p);
+  moda_fwd_tc_kernel<D, SC, NSLOT><<<grid, 384, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -614,13 +651,15 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.status = a.status;
-  // largest slot group whose staggered sub-slabs (one per position of a warp) fit a stage
+  // Prefer a 4-deep K/V ring (6-deep at d=64), then the largest depth slot group that fits.
   const int npos = positions_per_warp(pr.G, p.P);
-  auto fits = [&](int sc) { return npos * (sc * D * 2 + 16) <= kDepthStageBytes; };
-  if (fits(8)) return launch_cfg<D, 8>(p, tk, tv, s);
-  if (fits(4)) return launch_cfg<D, 4>(p, tk, tv, s);
-  if (fits(2)) return launch_cfg<D, 2>(p, tk, tv, s);
-  return launch_cfg<D, 1>(p, tk, tv, s);
+  constexpr int NS = D == 128 ? 4 : 6;
+  if (fits<D, 8, NS>(npos)) return launch_cfg<D, 8, NS>(p, npos, tk, tv, s);
+  if (fits<D, 4, NS>(npos)) return launch_cfg<D, 4, NS>(p, npos, tk, tv, s);
+  if (fits<D, 2, NS>(npos)) return launch_cfg<D, 2, NS>(p, npos, tk, tv, s);
+  if (fits<D, 1, NS>(npos)) return launch_cfg<D, 1, NS>(p, npos, tk, tv, s);
+  if (fits<D, 2, NS - 1>(npos)) return launch_cfg<D, 2, NS - 1>(p, npos, tk, tv, s);
+  return launch_cfg<D, 1, NS - 1>(p, npos, tk, tv, s);
 }
 
 }  // namespace
