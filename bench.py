@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""MoDA benchmark: one step = the whole hot path (forward + backward) on one batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints ONE JSON line (rank 0).  Our arm times K steps of moda_fwd + moda_bwd on
+device-resident synthetic inputs with CUDA events (max over ranks), then the same
+step end to end through the C ABI with pinned host buffers (H2D of the inputs,
+D2H of every output, inside the timed region).  The reference arm times the
+float64 CPU oracle on a bounded sample of the same workload.
+
+Under torchrun each rank runs an independent replica on its own GPU (the units,
+(batch, kv-head) problems, are independent: no data-path collective), so the
+reported value is the aggregate over ranks ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoDA fwd/bwd TFLOP/s and fraction of roofline (tensor peak vs HBM), 1×GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- counts
+def flops(shape):
+    """Algorithmic FLOPs: causal sequence part 4*B*H*d*T(T+1)/2 (QK^T and PV over the
+    visible triangle), depth part 4*B*H*T*S*d; backward counted as 2.5x forward."""
+    B, H, T, d, S = shape.B, shape.H, shape.T, shape.d, shape.S
+    seq = 4.0 * B * H * d * T * (T + 1) / 2
+    depth = 4.0 * B * H * T * S * d
+    return {"fwd_seq": seq, "fwd_depth": depth, "fwd": seq + depth, "bwd_seq": 2.5 * seq,
+            "bwd_depth": 2.5 * depth, "bwd": 2.5 * (seq + depth)}
+
+
+def bytes_moved(shape):
+    """Algorithmic HBM bytes: every tensor read or written once (depth KV once per kv head)."""
+    e = 2 if shape.dtype_name == "bf16" else 4
+    B, H, Hkv, T, d, S = shape.B, shape.H, shape.Hkv, shape.T, shape.d, shape.S
+    q = B * H * T * d * e
+    kv = 2 * B * Hkv * T * d * e
+    dkv = 2 * B * Hkv * T * S * d * e
+    lse = B * H * T * 4
+    fwd = q + kv + dkv + q + lse  # read q, k, v, kd, vd; write o, lse
+    bwd = (q + kv + dkv + q + q + lse) + (q + kv + dkv)  # read q,k,v,kd,vd,o,dout,lse; write dq..dvd
+    return {"fwd": fwd, "bwd": bwd, "inputs": q + kv + dkv + q, "outputs": q + lse + q + kv + dkv}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged
+    since the counters were taken (lines: kernel workload bytes source-sha256-prefix)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[3] == source_digest(kernel):
+                return float(parts[2])
+    return None
+
+
+KERNEL_SOURCES = {"moda_fwd_tc_kernel": ["moda_fwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_bwd": ["moda_bwd_sm103.cu", "moda_simt.cu", "sm103_ptx.cuh"]}
+
+
+def source_digest(kernel):
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES.get(kernel, []):
+        p = os.path.join(ROOT, "joint_sequence_depth_gb300", "csrc", fn)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle
+def oracle_sample(shape, T_sample):
+    """Bounded sample of the workload for the CPU oracle: batch 0, kv head 0 (its G query
+    heads), the first T_sample positions -- itself a valid MoDA problem."""
+    import numpy as np
+    import torch
+
+    from joint_sequence_depth_gb300.inputs import make_inputs, scaled
+
+    sub = scaled(shape, B=1, H=shape.G, Hkv=1, T=T_sample)
+    x = make_inputs(sub, seed=101, device="cpu", with_dout=True)
+    host = [x[n].view(torch.int16).numpy().view(np.uint16) if x[n].dtype == torch.bfloat16 else x[n].numpy()
+            for n in ("q", "k", "v", "kd", "vd", "dout")]
+    return sub, host
+
+
+def time_oracle_steps(shape, T_sample, steps):
+    import oracle
+
+    oracle.build()
+    sub, host = oracle_sample(shape, T_sample)
+    f = flops(sub)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.forward(*host[:5])
+        oracle.backward(*host)
+        times.append(time.perf_counter() - t0)
+    per = statistics.mean(times)
+    return {"value": (f["fwd"] + f["bwd"]) / per / 1e12, "seconds_per_step": per, "cores": oracle.cores(),
+            "sample": f"batch 0, kv head 0 ({sub.H} query heads), positions 0..{T_sample - 1}, "
+                      f"S={sub.S}, d={sub.d}: forward + backward ({(f['fwd'] + f['bwd']) / 1e9:.1f} GFLOP)"}
+
+
+# ----------------------------------------------------------------------------- main
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="bf16_train")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, shape):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    T_sample = 1024
+    time_oracle_steps(shape, T_sample, warm) if warm else None
+    r = time_oracle_steps(shape, T_sample, steps)
+    line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": r["seconds_per_step"] * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(shape),
+            "cpu_baseline": {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(shape):
+    return {"workload": f"{shape.name}: B={shape.B} H={shape.H} Hkv={shape.Hkv} T={shape.T} d={shape.d} "
+                        f"S={shape.S} {shape.dtype_name}, causal, forward+backward",
+            "global_batch": shape.B, "seq_len": shape.T, "depth_slots": shape.S,
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def main():
+    args = parse()
+    from joint_sequence_depth_gb300.inputs import SEEDS, WORKLOADS
+
+    base = WORKLOADS[args.workload]
+    shape = base
+    if args.impl == "reference":
+        return run_reference(args, shape)
+
+    import torch
+    import torch.distributed as dist
+
+    from joint_sequence_depth_gb300 import binding
+    from joint_sequence_depth_gb300 import build as mbuild
+    from joint_sequence_depth_gb300.inputs import make_inputs
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mbuild.build()
+    binding.load_library()
+
+    x = make_inputs(base, seed=SEEDS[args.workload] + 1000 * rank, device=dev, with_dout=True)
+    q, k, v, kd, vd, dout = (x[n] for n in ("q", "k", "v", "kd", "vd", "dout"))
+    o = torch.empty_like(q)
+    lse = torch.empty(base.B, base.H, base.T, dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(kd),
+             torch.empty_like(vd))
+    desc = binding.make_desc(base.B, base.H, base.Hkv, base.T, base.S, base.d, base.dtype)
+    ws = torch.empty(binding.moda_bwd_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.moda_fwd(q, k, v, kd, vd, o, lse)
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    launches0 = binding.moda_launch_count()
+    torch.cuda.synchronize()
+    for i in range(K):
+        ev[i][0].record(stream)
+        binding.moda_fwd(q, k, v, kd, vd, o, lse)
+        ev[i][1].record(stream)
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    launches = binding.moda_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    status = binding.moda_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(status, status)} after the timed steps")
+
+    # ------------------------------------------------------------- end to end (host buffers)
+    host_in = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "kd", "vd", "dout")}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse) + grads]
+    dev_in = {"q": q, "k": k, "v": v, "kd": kd, "vd": vd, "dout": dout}
+    E = max(1, args.e2e_steps)
+
+    def e2e_step():
+        for n, h in host_in.items():
+            dev_in[n].copy_(h, non_blocking=True)
+        step()
+        for h, d_ in zip(host_out, (o, lse) + grads):
+            h.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms, fwd_ms, bwd_ms = t.tolist()
+
+    f = flops(shape)
+    step_flops = f["fwd"] + f["bwd"]
+    ms_per_step = total_ms / K
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------------- roofline of the dominant kernel
+    peaks, peak_kind = load_peaks()
+    b = bytes_moved(shape)
+    if fwd_ms >= bwd_ms:
+        kernel, dur_ms, fl, by = "moda_fwd_tc_kernel", fwd_ms, f["fwd_seq"], b["fwd"]
+    else:
+        kernel, dur_ms, fl, by = "moda_bwd", bwd_ms, f["bwd_seq"], b["bwd"]
+    t_tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": fl / (dur_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / (dur_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_record(kernel, shape.name)
+    roof["kernel"] = kernel
+    roof["algorithmic"] = {"flops": fl, "bytes": by}
+    roof["peak_source"] = f"{peak_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'copy'})"
+    roof["step_share"] = dur_ms / (fwd_ms + bwd_ms)
+    roof["roofline_ms"] = max(t_tensor, t_hbm) * 1e3
+    roof["roofline_frac"] = max(t_tensor, t_hbm) * 1e3 / dur_ms
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle_steps(shape, shape.T, 1)
+        cpu = {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+                "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype_name, "data": "synthetic",
+                "config": workload_config(shape),
+                "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                "clocks": clk,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -107,6 +107,10 @@ const char* moda_status_str(moda_status status);
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t moda_version(void);
 
+/* Number of CUDA kernels this library has launched since it was loaded (all
+ * devices and streams; host-side count, no synchronisation). */
+int64_t moda_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

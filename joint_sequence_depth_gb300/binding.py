@@ -25,7 +25,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 # Names of every function include/moda.h declares.
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status", "moda_status_str",
-           "moda_version")
+           "moda_version", "moda_launch_count")
 
 
 class MODAError(RuntimeError):
@@ -64,6 +64,8 @@ def load_library():
             lib.moda_status_str.restype = ctypes.c_char_p
             lib.moda_version.argtypes = []
             lib.moda_version.restype = ctypes.c_int32
+            lib.moda_launch_count.argtypes = []
+            lib.moda_launch_count.restype = ctypes.c_int64
             _lib = lib
     return _lib
 
@@ -145,3 +147,8 @@ def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=No
 
 def moda_device_status(clear=True, stream=None) -> int:
     return int(load_library().moda_device_status(1 if clear else 0, _stream(stream)))
+
+
+def moda_launch_count() -> int:
+    """Kernels the library has launched since it was loaded."""
+    return int(load_library().moda_launch_count())

@@ -1,12 +1,20 @@
 // C ABI of the MoDA library (declared in include/moda.h): argument checks,
 // kernel selection and launches.  All compute runs in the kernels of this
 // directory; nothing here touches tensor data on the host.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 
 #include "moda.h"
 #include "moda_common.cuh"
+
+namespace moda {
+namespace {
+std::atomic<int64_t> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace moda
 
 namespace {
 
@@ -185,5 +193,7 @@ const char* moda_status_str(moda_status status) {
 }
 
 int32_t moda_version(void) { return 100; }
+
+int64_t moda_launch_count(void) { return moda::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -54,6 +54,9 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { retu
 // Records the first error code in the device status word (never traps).
 __device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, 0, code); }
 
+// Host-side count of kernels this library has launched (reported by moda_launch_count).
+void count_launches(int n);
+
 // Host-side launchers (one per kernel family).  Each returns the launch error.
 cudaError_t launch_fwd_simt(const FwdArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdArgs& a, int dtype, cudaStream_t s);

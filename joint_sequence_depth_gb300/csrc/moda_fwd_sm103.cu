@@ -626,6 +626,7 @@ cudaError_t launch_cfg(FwdTcParams p, int npos, const CUtensorMap& tk, const CUt
   }
   const unsigned grid = static_cast<unsigned>(p.n_pb) * p.B * p.Hkv;
   moda_fwd_tc_kernel<D, SC, NSLOT><<<grid, 384, smem, s>>>(tk, tv, p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -276,6 +276,7 @@ template <typename T, int D>
 cudaError_t fwd_simt(const FwdArgs& a, cudaStream_t s) {
   const unsigned grid = blocks_for(static_cast<int64_t>(a.p.B) * a.p.H, a.p.T);
   fwd_simt_kernel<T, D><<<grid, kWarps * 32, 0, s>>>(a);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -288,6 +289,7 @@ cudaError_t bwd_simt(const BwdArgs& a, cudaStream_t s) {
   if (a.p.S > 0)
     bwd_depth_simt_kernel<T, D>
         <<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
+  count_launches(a.p.S > 0 ? 4 : 3);
   return cudaGetLastError();
 }
 

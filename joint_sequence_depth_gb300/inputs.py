@@ -33,6 +33,10 @@ class Shape:
     def G(self) -> int:
         return self.H // self.Hkv
 
+    @property
+    def dtype_name(self) -> str:
+        return "bf16" if self.dtype == torch.bfloat16 else "f32"
+
 
 # The workloads MoDA is measured and checked on.
 WORKLOADS = {
