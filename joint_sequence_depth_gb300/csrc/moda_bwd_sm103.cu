@@ -1,0 +1,838 @@
+// MoDA backward for bf16 on sm_103a.  The pages give no backward; these kernels
+// evaluate the analytic gradient of the joint softmax (one denominator over the
+// causal sequence keys and the same-position depth slots, "Mixture-of-Depths
+// Attention", frame "One denominator allocates probability across both memories",
+// Sec. 2.2 / Algorithm 1).  With P = exp(score - LSE), Delta_t = dO_t . O_t and
+// dS = P (dO . value - Delta):
+//
+//   depth kernel (CUDA cores, warp per position):  dvd = sum_h P^d dO,
+//       dkd = scale sum_h dS^d q, and the depth share of dq (scale sum_i dS^d kd_i),
+//       kept in float32 in the workspace.
+//   dK/dV kernel (tcgen05, one CTA per 128 keys of a kv head, looping over 64-row
+//       query tiles of the G heads):  S^T = K Q^T, dP^T = V dO^T into TMEM;
+//       thread k (TMEM lane k) forms P^T and dS^T, written back to TMEM as bf16;
+//       dV += P^T dO, dK += dS^T Q with A read from TMEM.
+//   dQ kernel (tcgen05, one CTA per 128 expanded query rows, looping over 64-key
+//       tiles):  S = Q K^T, dP = dO V^T; thread r forms dS (bf16 into TMEM);
+//       dQ += dS K.  The epilogue adds the depth share and rounds to bf16.
+//
+// All waits are bounded (see sm103_ptx.cuh); a timeout records MODA_ERR_TIMEOUT.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "moda_common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace moda {
+namespace {
+
+using namespace sm103;
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
+  *abort_flag = 1;
+  record_status(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct BwdTcParams {
+  int B, H, Hkv, T, S, G;
+  float scale, scale_log2;
+  const __nv_bfloat16 *q, *k, *v, *kd, *vd, *dout;
+  const float* lse;
+  const float* delta;
+  float* dq_accum;  // depth share of dq, float32 [B,H,T,d] (read by the dQ kernel when S > 0)
+  __nv_bfloat16 *dq, *dk, *dv, *dkd, *dvd;
+  int* status;
+};
+
+// ============================================================================ depth
+// One warp per position (b, g, t).  Lane = (slot sub-index j, 16-byte column chunk cc):
+// a warp step covers SPW = 32 / (d/8) consecutive slots, each slot row read with one
+// coalesced 16-byte load per lane.  The G heads of the position (HG >= G) stay in
+// registers (q, dO packed bf16), so each depth element is read from HBM once and used
+// for all G heads.
+template <int D, int HG>
+__global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p) {
+  constexpr int CH = D / 8;
+  constexpr int SPW = 32 / CH;
+  const int lane = threadIdx.x & 31;
+  const int64_t pid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (pid >= static_cast<int64_t>(p.B) * p.Hkv * p.T) return;
+  const int t = static_cast<int>(pid % p.T);
+  const int64_t bg = pid / p.T;
+  const int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
+  const int j = lane / CH, cc = lane % CH;
+
+  uint4 qv[HG], dv4[HG];
+  float lse2[HG], dl[HG], dq[HG][8];
+#pragma unroll
+  for (int hh = 0; hh < HG; ++hh) {
+    const bool hv = hh < p.G;
+    const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + (hv ? hh : 0)) * p.T + t;
+    qv[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.q + row * D) + cc) : make_uint4(0, 0, 0, 0);
+    dv4[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.dout + row * D) + cc) : make_uint4(0, 0, 0, 0);
+    lse2[hh] = hv ? p.lse[row] * kLog2e : INFINITY;
+    dl[hh] = hv ? p.delta[row] : 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
+  }
+  const int64_t slab = pid * p.S * D;
+  for (int i0 = 0; i0 < p.S; i0 += SPW) {
+    const int i = i0 + j;
+    const bool sv = i < p.S;
+    const uint4 kv = sv ? __ldg(reinterpret_cast<const uint4*>(p.kd + slab + static_cast<int64_t>(i) * D) + cc)
+                        : make_uint4(0, 0, 0, 0);
+    const uint4 vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
+                        : make_uint4(0, 0, 0, 0);
+    float s[HG], dp[HG];
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) {
+      float a = 0.f, c2 = 0.f;
+      a = dot2_bf16(qv[hh].x, kv.x, a);
+      a = dot2_bf16(qv[hh].y, kv.y, a);
+      a = dot2_bf16(qv[hh].z, kv.z, a);
+      a = dot2_bf16(qv[hh].w, kv.w, a);
+      c2 = dot2_bf16(dv4[hh].x, vv.x, c2);
+      c2 = dot2_bf16(dv4[hh].y, vv.y, c2);
+      c2 = dot2_bf16(dv4[hh].z, vv.z, c2);
+      c2 = dot2_bf16(dv4[hh].w, vv.w, c2);
+      s[hh] = a;
+      dp[hh] = c2;
+    }
+    // full dot products: reduce over the CH lanes of this slot
+#pragma unroll
+    for (int off = CH / 2; off >= 1; off >>= 1) {
+#pragma unroll
+      for (int hh = 0; hh < HG; ++hh) {
+        s[hh] += __shfl_xor_sync(0xffffffffu, s[hh], off);
+        dp[hh] += __shfl_xor_sync(0xffffffffu, dp[hh], off);
+      }
+    }
+    float kf[8], vf[8];
+    {
+      const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        kf[2 * c] = bf16_lo(kw[c]);
+        kf[2 * c + 1] = bf16_hi(kw[c]);
+        vf[2 * c] = bf16_lo(vw[c]);
+        vf[2 * c + 1] = bf16_hi(vw[c]);
+      }
+    }
+    float gk[8], gv[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) gk[c] = gv[c] = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) {
+      const float pr = sv ? ex2(fmaf(s[hh], p.scale_log2, -lse2[hh])) : 0.f;
+      const float ds = pr * (dp[hh] - dl[hh]);
+      const uint32_t qw[4] = {qv[hh].x, qv[hh].y, qv[hh].z, qv[hh].w};
+      const uint32_t ow[4] = {dv4[hh].x, dv4[hh].y, dv4[hh].z, dv4[hh].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        gk[2 * c] = fmaf(ds, bf16_lo(qw[c]), gk[2 * c]);
+        gk[2 * c + 1] = fmaf(ds, bf16_hi(qw[c]), gk[2 * c + 1]);
+        gv[2 * c] = fmaf(pr, bf16_lo(ow[c]), gv[2 * c]);
+        gv[2 * c + 1] = fmaf(pr, bf16_hi(ow[c]), gv[2 * c + 1]);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dq[hh][c] = fmaf(ds, kf[c], dq[hh][c]);
+    }
+    if (sv) {
+      uint4 ok, ov;
+      ok.x = pack_bf16(gk[0] * p.scale, gk[1] * p.scale);
+      ok.y = pack_bf16(gk[2] * p.scale, gk[3] * p.scale);
+      ok.z = pack_bf16(gk[4] * p.scale, gk[5] * p.scale);
+      ok.w = pack_bf16(gk[6] * p.scale, gk[7] * p.scale);
+      ov.x = pack_bf16(gv[0], gv[1]);
+      ov.y = pack_bf16(gv[2], gv[3]);
+      ov.z = pack_bf16(gv[4], gv[5]);
+      ov.w = pack_bf16(gv[6], gv[7]);
+      reinterpret_cast<uint4*>(p.dkd + slab + static_cast<int64_t>(i) * D)[cc] = ok;
+      reinterpret_cast<uint4*>(p.dvd + slab + static_cast<int64_t>(i) * D)[cc] = ov;
+    }
+  }
+  // dq depth share: reduce over the SPW slot groups, lanes of group 0 write float32
+#pragma unroll
+  for (int off = CH; off < 32; off <<= 1) {
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dq[hh][c] += __shfl_xor_sync(0xffffffffu, dq[hh][c], off);
+  }
+  if (j == 0) {
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) {
+      if (hh < p.G) {
+        const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + t;
+        float4* dst = reinterpret_cast<float4*>(p.dq_accum + row * D + cc * 8);
+        dst[0] = make_float4(dq[hh][0] * p.scale, dq[hh][1] * p.scale, dq[hh][2] * p.scale, dq[hh][3] * p.scale);
+        dst[1] = make_float4(dq[hh][4] * p.scale, dq[hh][5] * p.scale, dq[hh][6] * p.scale, dq[hh][7] * p.scale);
+      }
+    }
+  }
+}
+
+// ============================================================================ dQ
+// CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G,
+// head g*G + r%G), P = floor(128/G) positions.  Keys in tiles of 64.
+// Warps: 0 TMA (K_j, V_j), 1 MMA + TMEM, 4..11 two gradient warpgroups (WG w handles
+// key columns [32w, 32w+32) of every tile; WG 0 also loads Q and dO rows).
+// TMEM: S[2] cols [0,64) [64,128), dP[2] [128,192) [192,256), dQ [256, 256+d).
+// dS (bf16) is written over the first 32 columns of S[j%2].
+constexpr int QBM = 128, QBN = 64;
+
+template <int D>
+struct DqCfg {
+  static constexpr int KV_BYTES = QBN * D * 2;
+  static constexpr int NSLOT = D == 128 ? 6 : 8;
+  static constexpr int Q_BYTES = QBM * D * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = Q_BYTES;
+  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[2], ds_full[2], dq_done[2], drain
+  static constexpr int NBAR = 2 * NSLOT + 8;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    moda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const BwdTcParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kStatusConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = QBM / p.G;
+  const int n_pb = (p.T + P - 1) / P;
+  const int ngroups = p.B * p.Hkv;
+  const int pb = n_pb - 1 - static_cast<int>(blockIdx.x) / ngroups;
+  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int p0 = pb * P;
+  const int p_last = min(p0 + P, p.T) - 1;
+  const int n_kv = p_last / QBN + 1;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + C::NSLOT;
+  uint64_t* q_full = bars + 2 * C::NSLOT;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* ds_full = s_full + 2;
+  uint64_t* dq_done = ds_full + 2;
+  uint64_t* drain = dq_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_full, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&ds_full[i], 256);
+      mbar_init(&dq_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // items K0, V0, K1, V1, ...; V_j is released after dP_j, K_j after dQ_j
+      int issued = 0;
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int slot = it % C::NSLOT, use = it / C::NSLOT;
+        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
+          raise_abort(abort_flag, p.status);
+          break;
+        }
+        const CUtensorMap* map = (it & 1) ? &tmV : &tmK;
+        uint8_t* dst = smem + C::OFF_KV + slot * C::KV_BYTES;
+        mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(dst + h * (QBN * 128), map, &kv_full[slot], h * 64, (it >> 1) * QBN, bg);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        for (int it = max(0, issued - C::NSLOT); it < issued; ++it)
+          mbar_wait(&kv_full[it % C::NSLOT], (it / C::NSLOT) & 1, &never);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(QBM, QBN, false);
+      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
+      const uint32_t q_base = sbase + C::OFF_Q, do_base = sbase + C::OFF_DO;
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      auto issue_s = [&](int j) -> bool {
+        const int sk = (2 * j) % C::NSLOT, sv = (2 * j + 1) % C::NSLOT;
+        if (!mbar_wait(&kv_full[sk], ((2 * j) / C::NSLOT) & 1, abort_flag)) return false;
+        if (!mbar_wait(&kv_full[sv], ((2 * j + 1) / C::NSLOT) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t k_base = sbase + C::OFF_KV + sk * C::KV_BYTES;
+        const uint32_t v_base = sbase + C::OFF_KV + sv * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (QBM * 128) + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TM_S + (j & 1) * QBN, sdesc_sw128(q_base + aoff, 16, 1024),
+                      sdesc_sw128(k_base + boff, 16, 1024), IDESC_S, kk > 0);
+          mma_bf16_ss(tmem + C::TM_DP + (j & 1) * QBN, sdesc_sw128(do_base + aoff, 16, 1024),
+                      sdesc_sw128(v_base + boff, 16, 1024), IDESC_S, kk > 0);
+        }
+        mma_commit(&s_full[j & 1]);
+        mma_commit(&kv_empty[sv]);
+        return true;
+      };
+      auto issue_dq = [&](int j) -> bool {
+        if (!mbar_wait(&ds_full[j & 1], (j >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const int sk = (2 * j) % C::NSLOT;
+        const uint32_t k_base = sbase + C::OFF_KV + sk * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < QBN / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + (j & 1) * QBN + kk * 8,
+                      sdesc_sw128(k_base + kk * 16 * 128, QBN * 128, 1024), IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&dq_done[j & 1]);
+        mma_commit(&kv_empty[sk]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_kv > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        ok = issue_dq(j);
+        if (ok && j + 2 < n_kv) ok = issue_s(j + 2);
+      }
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;  // 0 or 1: key columns [32*wg, 32*wg + 32)
+    const int r = ((warp & 3) << 5) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int pos = p0 + r / p.G;
+    const bool valid = (r < P * p.G) && pos < p.T;
+    const int h = g * p.G + r % p.G;
+    const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
+    if (wg == 0) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
+      const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {
+        const uint32_t off = (ch >> 3) * (QBM * 128) + sw128_offset(r, ch & 7);
+        st_shared_v4(sbase + C::OFF_Q + off, valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0));
+        st_shared_v4(sbase + C::OFF_DO + off, valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0));
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const float lse2 = valid ? p.lse[row] * kLog2e : INFINITY;
+    const float dlt = valid ? p.delta[row] : 0.f;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = warp_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[32], dpv[32];
+      tmem_ld32(tmem + lane_base + C::TM_S + (j & 1) * QBN + wg * 32, s);
+      tmem_ld32(tmem + lane_base + C::TM_DP + (j & 1) * QBN + wg * 32, dpv);
+      const int kb = j * QBN + wg * 32;
+      const int lim = valid ? pos - kb : -1;  // columns c <= lim are visible
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float e0 = ex2(fmaf(__uint_as_float(s[c]), sl2, -lse2));
+        float e1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -lse2));
+        e0 = (c <= lim) ? e0 : 0.f;
+        e1 = (c + 1 <= lim) ? e1 : 0.f;
+        const float d0 = e0 * (__uint_as_float(dpv[c]) - dlt);
+        const float d1 = e1 * (__uint_as_float(dpv[c + 1]) - dlt);
+        pk[c >> 1] = pack_bf16(d0, d1);
+      }
+      // dS (bf16 pairs) into columns [16*wg, 16*wg+16) of S[j%2]
+      tmem_st16(tmem + lane_base + C::TM_S + (j & 1) * QBN + wg * 16, pk);
+      tc_fence_before();
+      mbar_arrive(&ds_full[j & 1]);
+    }
+    if (!ok) {
+      raise_abort(abort_flag, p.status);
+    } else {
+      const int jl = n_kv - 1;
+      ok = warp_wait(&dq_done[jl & 1], (jl >> 1) & 1, abort_flag);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+      } else {
+        tc_fence_after();
+        // WG w writes dq columns [w*D/2, (w+1)*D/2)
+#pragma unroll 1
+        for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+          uint32_t acc[32];
+          tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
+          float extra[32];
+          if (p.S > 0 && valid) {
+            const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 e = src[i];
+              extra[4 * i] = e.x;
+              extra[4 * i + 1] = e.y;
+              extra[4 * i + 2] = e.z;
+              extra[4 * i + 3] = e.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                const int c = 8 * i + 2 * k2;
+                w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
+                                  fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
+              }
+              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================ dK / dV
+// CTA: 128 keys [kb, kb+128) of (b, g).  Query tiles of 64 rows, head-major inside the
+// tile (row r -> head g*G + r/P', position p0 + r%P', P' = floor(64/G)), loaded by TMA
+// together with dO; their LSE (log2 units) and Delta are staged by the producer warp.
+// Warps: 0 TMA + row statistics, 1 MMA + TMEM, 4..11 two gradient warpgroups (WG w
+// handles query columns [32w, 32w+32)); thread = key (TMEM lane).
+// TMEM: S^T[2] cols [0,64) [64,128), dP^T[2] [128,192) [192,256), dV [256,256+d),
+// dK [256+d, 256+2d).  P^T and dS^T (bf16) overwrite the first 32 columns of their buffers.
+constexpr int KBM = 128, KBN = 64;
+
+template <int D>
+struct DkvCfg {
+  static constexpr int KV_BYTES = KBM * D * 2;   // the CTA's K (or V) tile
+  static constexpr int QT_BYTES = KBN * D * 2;   // one 64-row Q (or dO) tile
+  static constexpr int NSTAGE = 4;
+  static constexpr int STAGE_BYTES = 2 * QT_BYTES;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_BYTES;
+  static constexpr int OFF_Q = 2 * KV_BYTES;     // stage s: Q at + s*STAGE, dO at + QT_BYTES
+  static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][2][64] floats
+  static constexpr int OFF_BAR = OFF_STAT + NSTAGE * 2 * KBN * 4;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], p_full[2], g_done[2], drain
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    moda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                         const BwdTcParams p) {
+  using C = DkvCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kStatusConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Pq = KBN / p.G;  // positions per query tile
+  const int n_kb = (p.T + KBM - 1) / KBM;
+  const int ngroups = p.B * p.Hkv;
+  const int kblk = static_cast<int>(blockIdx.x) / ngroups;  // smallest key blocks (most query tiles) first
+  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int kb = kblk * KBM;
+  const int qt0 = kb / Pq, qt1 = (p.T - 1) / Pq;
+  const int n_q = qt1 - qt0 + 1;
+  (void)n_kb;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::NSTAGE;
+  uint64_t* s_full = q_empty + C::NSTAGE;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* g_done = p_full + 2;
+  uint64_t* drain = g_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 256);
+      mbar_init(&g_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // rows past Pq*G of every query tile are never written by TMA: zero them once
+  if (Pq * p.G < KBN) {
+    for (int i = threadIdx.x; i < C::NSTAGE * C::STAGE_BYTES / 16; i += blockDim.x)
+      st_shared_v4(sbase + C::OFF_Q + i * 16, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- loads
+    bool ok = true;
+    int issued = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(smem + C::OFF_K + h * (KBM * 128), &tmK, kv_full, h * 64, kb, bg);
+        tma_load_3d(smem + C::OFF_V + h * (KBM * 128), &tmV, kv_full, h * 64, kb, bg);
+      }
+    }
+    for (int i = 0; i < n_q; ++i) {
+      const int st = i % C::NSTAGE, use = i / C::NSTAGE;
+      if (use > 0 && !warp_wait(&q_empty[st], (use - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int p0 = (qt0 + i) * Pq;
+      // row statistics of this tile: lse in log2 units (+inf for rows that do not exist), Delta
+      float* sl = stat + st * 2 * KBN;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = lane + 32 * rr;
+        const int hh = r / Pq, pos = p0 + r % Pq;
+        const bool valid = hh < p.G && pos < p.T;
+        const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + (valid ? hh : 0)) * p.T + (valid ? pos : 0);
+        sl[r] = valid ? p.lse[row] * kLog2e : INFINITY;
+        sl[KBN + r] = valid ? p.delta[row] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* dst = smem + C::OFF_Q + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&q_full[st], static_cast<uint32_t>(2 * Pq * p.G * D * 2));
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(dst + h * (KBN * 128), &tmQ, &q_full[st], h * 64, p0, b * p.H + g * p.G);
+          tma_load_3d(dst + C::QT_BYTES + h * (KBN * 128), &tmO, &q_full[st], h * 64, p0, b * p.H + g * p.G);
+        }
+      }
+      issued = i + 1;
+    }
+    if (!ok || *abort_flag) {
+      if (lane == 0) {
+        raise_abort(abort_flag, p.status);
+        volatile int never = 0;
+        mbar_wait(kv_full, 0, &never);
+        for (int i = max(0, issued - C::NSTAGE); i < issued; ++i)
+          mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(KBM, KBN, false);
+      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
+      const uint32_t k_base = sbase + C::OFF_K, v_base = sbase + C::OFF_V;
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % C::NSTAGE;
+        if (!mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t q_base = sbase + C::OFF_Q + st * C::STAGE_BYTES, o_base = q_base + C::QT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (KBM * 128) + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * (KBN * 128) + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TM_S + (i & 1) * KBN, sdesc_sw128(k_base + aoff, 16, 1024),
+                      sdesc_sw128(q_base + boff, 16, 1024), IDESC_S, kk > 0);
+          mma_bf16_ss(tmem + C::TM_DP + (i & 1) * KBN, sdesc_sw128(v_base + aoff, 16, 1024),
+                      sdesc_sw128(o_base + boff, 16, 1024), IDESC_S, kk > 0);
+        }
+        mma_commit(&s_full[i & 1]);
+        return true;
+      };
+      auto issue_g = [&](int i) -> bool {
+        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const int st = i % C::NSTAGE;
+        const uint32_t q_base = sbase + C::OFF_Q + st * C::STAGE_BYTES, o_base = q_base + C::QT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < KBN / 16; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + (i & 1) * KBN + kk * 8,
+                      sdesc_sw128(o_base + kk * 16 * 128, KBN * 128, 1024), IDESC_G, acc);
+          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + (i & 1) * KBN + kk * 8,
+                      sdesc_sw128(q_base + kk * 16 * 128, KBN * 128, 1024), IDESC_G, acc);
+        }
+        mma_commit(&g_done[i & 1]);
+        mma_commit(&q_empty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_q > 1) ok = issue_s(1);
+      for (int i = 0; ok && i < n_q; ++i) {
+        ok = issue_g(i);
+        if (ok && i + 2 < n_q) ok = issue_s(i + 2);
+      }
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- gradients (thread = key)
+    const int wg = (warp - 4) >> 2;
+    const int kr = ((warp & 3) << 5) + lane;
+    const int key = kb + kr;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n_q; ++i) {
+      ok = warp_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[32], dpv[32];
+      tmem_ld32(tmem + lane_base + C::TM_S + (i & 1) * KBN + wg * 32, s);
+      tmem_ld32(tmem + lane_base + C::TM_DP + (i & 1) * KBN + wg * 32, dpv);
+      const int st = i % C::NSTAGE;
+      const float* sl = stat + st * 2 * KBN + wg * 32;
+      const int p0 = (qt0 + i) * Pq;
+      const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
+      uint32_t pp[16], pd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float e[2], dd[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = wg * 32 + c + u;
+          float x = ex2(fmaf(__uint_as_float(s[c + u]), sl2, -sl[c + u]));
+          if (diag && key > p0 + r % Pq) x = 0.f;
+          e[u] = x;
+          dd[u] = x * (__uint_as_float(dpv[c + u]) - sl[KBN + c + u]);
+        }
+        pp[c >> 1] = pack_bf16(e[0], e[1]);
+        pd[c >> 1] = pack_bf16(dd[0], dd[1]);
+      }
+      tmem_st16(tmem + lane_base + C::TM_S + (i & 1) * KBN + wg * 16, pp);
+      tmem_st16(tmem + lane_base + C::TM_DP + (i & 1) * KBN + wg * 16, pd);
+      tc_fence_before();
+      mbar_arrive(&p_full[i & 1]);
+    }
+    if (!ok) {
+      raise_abort(abort_flag, p.status);
+    } else {
+      const int il = n_q - 1;
+      ok = warp_wait(&g_done[il & 1], (il >> 1) & 1, abort_flag);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+      } else {
+        tc_fence_after();
+        // WG 0 writes dV, WG 1 writes dK (scaled)
+        const uint32_t src = wg == 0 ? C::TM_DV : C::TM_DK;
+        __nv_bfloat16* out = (wg == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
+        const float mul = wg == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t acc[32];
+          tmem_ld32(tmem + lane_base + src + c0, acc);
+          if (key < p.T) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pack_bf16(__uint_as_float(acc[8 * u]) * mul, __uint_as_float(acc[8 * u + 1]) * mul),
+                                  pack_bf16(__uint_as_float(acc[8 * u + 2]) * mul, __uint_as_float(acc[8 * u + 3]) * mul),
+                                  pack_bf16(__uint_as_float(acc[8 * u + 4]) * mul, __uint_as_float(acc[8 * u + 5]) * mul),
+                                  pack_bf16(__uint_as_float(acc[8 * u + 6]) * mul, __uint_as_float(acc[8 * u + 7]) * mul));
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [planes][T][D] as the 3-D tensor (D, T, planes), box 64 x rows x depth, 128-byte
+// swizzle, out-of-range rows read as zeros.
+bool make_map(CUtensorMap* map, const void* base, int D, int T, int planes, int rows, int depth) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(T) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(depth)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes, int& done) {
+  if (done >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done = bytes;
+  return e;
+}
+
+template <int D>
+cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
+  const Problem& pr = a.p;
+  BwdTcParams p;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.Hkv = pr.Hkv;
+  p.T = pr.T;
+  p.S = pr.S;
+  p.G = pr.G;
+  p.scale = pr.scale;
+  p.scale_log2 = pr.scale_log2;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k);
+  p.v = static_cast<const __nv_bfloat16*>(a.v);
+  p.kd = static_cast<const __nv_bfloat16*>(a.kd);
+  p.vd = static_cast<const __nv_bfloat16*>(a.vd);
+  p.dout = static_cast<const __nv_bfloat16*>(a.dout);
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq_accum = a.dq_accum;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.dkd = static_cast<__nv_bfloat16*>(a.dkd);
+  p.dvd = static_cast<__nv_bfloat16*>(a.dvd);
+  p.status = a.status;
+
+  cudaError_t e = launch_bwd_delta(a, 1, s);
+  if (e != cudaSuccess) return e;
+  const int64_t positions = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;
+  if (pr.S > 0) {
+    const unsigned grid = static_cast<unsigned>((positions + 7) / 8);
+    if (pr.G == 1) moda_bwd_depth_kernel<D, 1><<<grid, 256, 0, s>>>(p);
+    else if (pr.G == 2) moda_bwd_depth_kernel<D, 2><<<grid, 256, 0, s>>>(p);
+    else if (pr.G <= 4) moda_bwd_depth_kernel<D, 4><<<grid, 256, 0, s>>>(p);
+    else moda_bwd_depth_kernel<D, 8><<<grid, 256, 0, s>>>(p);
+    count_launches(1);
+  }
+  CUtensorMap tk128, tv128, tk64, tv64, tq, to;
+  const int planes_kv = pr.B * pr.Hkv, planes_q = pr.B * pr.H;
+  const int pq = KBN / pr.G;
+  if (!make_map(&tk128, a.k, D, pr.T, planes_kv, KBM, 1) || !make_map(&tv128, a.v, D, pr.T, planes_kv, KBM, 1) ||
+      !make_map(&tk64, a.k, D, pr.T, planes_kv, QBN, 1) || !make_map(&tv64, a.v, D, pr.T, planes_kv, QBN, 1) ||
+      !make_map(&tq, a.q, D, pr.T, planes_q, pq, pr.G) || !make_map(&to, a.dout, D, pr.T, planes_q, pq, pr.G))
+    return cudaErrorInvalidValue;
+  static int smem_dkdv = 0, smem_dq = 0;
+  e = set_smem(moda_bwd_dkdv_kernel<D>, DkvCfg<D>::SMEM, smem_dkdv);
+  if (e != cudaSuccess) return e;
+  e = set_smem(moda_bwd_dq_kernel<D>, DqCfg<D>::SMEM, smem_dq);
+  if (e != cudaSuccess) return e;
+  const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
+  moda_bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::SMEM, s>>>(tk128, tv128, tq, to, p);
+  const int P = QBM / pr.G;
+  const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
+  moda_bwd_dq_kernel<D><<<grid_q, 384, DqCfg<D>::SMEM, s>>>(tk64, tv64, p);
+  count_launches(2);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// bf16, d in {64, 128}, 1 <= G <= 8 (the depth kernel keeps a position's G heads in registers).
+bool bwd_sm103_supported(const Problem& p) { return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= 8; }
+
+cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s) {
+  return a.p.d == 64 ? launch_all<64>(a, s) : launch_all<128>(a, s);
+}
+
+}  // namespace moda

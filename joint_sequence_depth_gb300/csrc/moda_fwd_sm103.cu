@@ -671,8 +671,4 @@ cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {
   return a.p.d == 64 ? launch<64>(a, s) : launch<128>(a, s);
 }
 
-bool bwd_sm103_supported(const Problem&) { return false; }
-
-cudaError_t launch_bwd_sm103(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-
 }  // namespace moda

@@ -300,6 +300,20 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, int dtype, cudaStream_t s) {
   return a.p.d == 64 ? fwd_simt<__nv_bfloat16, 64>(a, s) : fwd_simt<__nv_bfloat16, 128>(a, s);
 }
 
+cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.p.B) * a.p.H * a.p.T;
+  const unsigned grid = static_cast<unsigned>((rows + kWarps - 1) / kWarps);
+  if (dtype == 0) {
+    if (a.p.d == 64) bwd_delta_kernel<float, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else bwd_delta_kernel<float, 128><<<grid, kWarps * 32, 0, s>>>(a);
+  } else {
+    if (a.p.d == 64) bwd_delta_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else bwd_delta_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, s>>>(a);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_simt(const BwdArgs& a, int dtype, cudaStream_t s) {
   if (dtype == 0) return a.p.d == 64 ? bwd_simt<float, 64>(a, s) : bwd_simt<float, 128>(a, s);
   return a.p.d == 64 ? bwd_simt<__nv_bfloat16, 64>(a, s) : bwd_simt<__nv_bfloat16, 128>(a, s);
