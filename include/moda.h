@@ -97,6 +97,24 @@ moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const 
                      const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                      void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream);
 
+/* moda_bwd for callers that cannot allocate device memory (allocator hooks, runtimes
+ * with a device-memory budget fixed at start-up, plain-C callers without an
+ * allocator).  The paper has no counterpart: this is a library convenience.
+ * Same arguments and results as moda_bwd minus the workspace, which is taken from a
+ * fixed array of moda_bwd_noalloc_max_workspace_bytes() (32 MiB) inside the
+ * library's device image; nothing is allocated.  Problems whose
+ * moda_bwd_workspace_bytes exceeds that size return MODA_ERR_WORKSPACE without
+ * launching.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and must therefore precede any stream capture on that
+ * device.  Every call shares the array: calls that overlap on the GPU race and must
+ * be serialised by the caller. */
+moda_status moda_bwd_noalloc(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                             const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                             void* dv, void* dkd, void* dvd, void* stream);
+
+/* Size in bytes of the fixed scratch array moda_bwd_noalloc uses. */
+size_t moda_bwd_noalloc_max_workspace_bytes(void);
+
 /* Reads the device status word that bounded waits write (MODA_OK when clean) and,
  * when `clear` is non-zero, resets it.  Waits for `stream` first. */
 moda_status moda_device_status(int clear, void* stream);

@@ -25,7 +25,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 # Names of every function include/moda.h declares.
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status", "moda_status_str",
-           "moda_version", "moda_launch_count")
+           "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes")
 
 
 class MODAError(RuntimeError):
@@ -66,6 +66,10 @@ def load_library():
             lib.moda_version.restype = ctypes.c_int32
             lib.moda_launch_count.argtypes = []
             lib.moda_launch_count.restype = ctypes.c_int64
+            lib.moda_bwd_noalloc.argtypes = [d] + [p] * 14
+            lib.moda_bwd_noalloc.restype = ctypes.c_int
+            lib.moda_bwd_noalloc_max_workspace_bytes.argtypes = []
+            lib.moda_bwd_noalloc_max_workspace_bytes.restype = ctypes.c_size_t
             _lib = lib
     return _lib
 
@@ -152,3 +156,22 @@ def moda_device_status(clear=True, stream=None) -> int:
 def moda_launch_count() -> int:
     """Kernels the library has launched since it was loaded."""
     return int(load_library().moda_launch_count())
+
+
+def moda_bwd_noalloc(q, k, v, kd, vd, o, lse, dout, grads, scale=None, stream=None):
+    """moda_bwd without a workspace argument, for callers that cannot allocate device memory:
+    the library uses its own fixed device array (see include/moda.h).  ``grads`` must be
+    preallocated (dq, dk, dv, dkd, dvd); returns them."""
+    desc = _desc_from(q, k, kd, scale)
+    dq, dk, dv, dkd, dvd = grads
+    st = load_library().moda_bwd_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None, _ptr(vd) if desc.S else None,
+        _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkd) if desc.S else None,
+        _ptr(dvd) if desc.S else None, _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_bwd_noalloc")
+    return grads
+
+
+def moda_bwd_noalloc_max_workspace_bytes() -> int:
+    return int(load_library().moda_bwd_noalloc_max_workspace_bytes())
