@@ -82,13 +82,20 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
     for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
   }
   const int64_t slab = pid * p.S * D;
+  auto load_slot = [&](int i, uint4& kv, uint4& vv) {
+    const bool sv = i < p.S;
+    kv = sv ? __ldg(reinterpret_cast<const uint4*>(p.kd + slab + static_cast<int64_t>(i) * D) + cc)
+            : make_uint4(0, 0, 0, 0);
+    vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
+            : make_uint4(0, 0, 0, 0);
+  };
+  uint4 kn, vn;  // next step's slot rows, loaded one step ahead
+  load_slot(j, kn, vn);
   for (int i0 = 0; i0 < p.S; i0 += SPW) {
     const int i = i0 + j;
     const bool sv = i < p.S;
-    const uint4 kv = sv ? __ldg(reinterpret_cast<const uint4*>(p.kd + slab + static_cast<int64_t>(i) * D) + cc)
-                        : make_uint4(0, 0, 0, 0);
-    const uint4 vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
-                        : make_uint4(0, 0, 0, 0);
+    const uint4 kv = kn, vv = vn;
+    if (i0 + SPW < p.S) load_slot(i + SPW, kn, vn);
     float s[HG], dp[HG];
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {
@@ -181,33 +188,39 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 // ============================================================================ dQ
 // CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G,
 // head g*G + r%G), P = floor(128/G) positions.  Keys in tiles of 64.
-// Warps: 0 TMA (K_j, V_j), 1 MMA + TMEM, 4..11 two gradient warpgroups (WG w handles
-// key columns [32w, 32w+32) of every tile; WG 0 also loads Q and dO rows).
-// TMEM: S[2] cols [0,64) [64,128), dP[2] [128,192) [192,256), dQ [256, 256+d).
-// dS (bf16) is written over the first 32 columns of S[j%2].
+// Warps: 0 TMA (K_j and V_j in one transaction), 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient
+// warps (warp w owns TMEM lanes 32*(w%4) ..; with two warpgroups WG k handles key
+// columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also loads Q
+// and dO).  NBUF S/dP buffers: with 2 the tensor cores compute tile j+1 while tile j's
+// dS is formed; with 1 (d = 64) the TMEM footprint is 256 columns so two CTAs share an
+// SM and overlap each other instead.
+// TMEM: S[b] cols [64b, 64b+64), dP[b] [64(NBUF+b), ...), dQ [128 NBUF, 128 NBUF + d).
+// dS (bf16) is written over the first 32 columns of S[b].
 constexpr int QBM = 128, QBN = 64;
 
-template <int D>
+template <int D, int NBUF, int NWG>
 struct DqCfg {
-  static constexpr int KV_BYTES = QBN * D * 2;
-  static constexpr int NSLOT = D == 128 ? 6 : 8;
+  static constexpr int THREADS = 64 + 128 * NWG;
+  static constexpr int KV_BYTES = QBN * D * 2;  // one K (or V) tile; a ring slot holds both
+  static constexpr int NSLOT = NBUF == 2 ? 3 : 4;
   static constexpr int Q_BYTES = QBM * D * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = Q_BYTES;
   static constexpr int OFF_KV = 2 * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[2], ds_full[2], dq_done[2], drain
-  static constexpr int NBAR = 2 * NSLOT + 8;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[NBUF], ds_full[NBUF], drain, last_done
+  static constexpr int NBAR = 2 * NSLOT + 3 + 2 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+  static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DQ = 128 * NBUF;
+  static constexpr uint32_t TM_COLS = (TM_DQ + D) <= 256 ? 256 : 512;
 };
 
-template <int D>
-__global__ void __launch_bounds__(384, 1)
+template <int D, int NBUF, int NWG>
+__global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 1)
     moda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const BwdTcParams p) {
-  using C = DqCfg<D>;
+  using C = DqCfg<D, NBUF, NWG>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
@@ -230,9 +243,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* kv_empty = bars + C::NSLOT;
   uint64_t* q_full = bars + 2 * C::NSLOT;
   uint64_t* s_full = q_full + 1;
-  uint64_t* ds_full = s_full + 2;
-  uint64_t* dq_done = ds_full + 2;
-  uint64_t* drain = dq_done + 2;
+  uint64_t* ds_full = s_full + NBUF;
+  uint64_t* drain = ds_full + NBUF;
+  uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -242,12 +255,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(q_full, 128);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 256);
-      mbar_init(&dq_done[i], 1);
+      mbar_init(&ds_full[i], 128 * NWG);
     }
     mbar_init(drain, 1);
+    mbar_init(last_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tmap(&tmV);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -265,74 +278,80 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- K_j, V_j loads
     if (lane == 0) {
-      // items K0, V0, K1, V1, ...; V_j is released after dP_j, K_j after dQ_j
       int issued = 0;
-      for (int it = 0; it < 2 * n_kv; ++it) {
-        const int slot = it % C::NSLOT, use = it / C::NSLOT;
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j % C::NSLOT, use = j / C::NSLOT;
         if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
           raise_abort(abort_flag, p.status);
           break;
         }
-        const CUtensorMap* map = (it & 1) ? &tmV : &tmK;
-        uint8_t* dst = smem + C::OFF_KV + slot * C::KV_BYTES;
-        mbar_arrive_expect_tx(&kv_full[slot], C::KV_BYTES);
+        uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
+        mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(dst + h * (QBN * 128), map, &kv_full[slot], h * 64, (it >> 1) * QBN, bg);
-        issued = it + 1;
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(dst + h * (QBN * 128), &tmK, &kv_full[slot], h * 64, j * QBN, bg);
+          tma_load_3d(dst + C::KV_BYTES + h * (QBN * 128), &tmV, &kv_full[slot], h * 64, j * QBN, bg);
+        }
+        issued = j + 1;
       }
       if (*abort_flag) {
         volatile int never = 0;
-        for (int it = max(0, issued - C::NSLOT); it < issued; ++it)
-          mbar_wait(&kv_full[it % C::NSLOT], (it / C::NSLOT) & 1, &never);
+        for (int j = max(0, issued - C::NSLOT); j < issued; ++j)
+          mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, QBN, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
-      const uint32_t q_base = sbase + C::OFF_Q, do_base = sbase + C::OFF_DO;
+      // descriptors built once; each MMA only advances the start address
+      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t do_desc = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
+      const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, QBN * 128, 1024);    // MN-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_s = [&](int j) -> bool {
-        const int sk = (2 * j) % C::NSLOT, sv = (2 * j + 1) % C::NSLOT;
-        if (!mbar_wait(&kv_full[sk], ((2 * j) / C::NSLOT) & 1, abort_flag)) return false;
-        if (!mbar_wait(&kv_full[sv], ((2 * j + 1) / C::NSLOT) & 1, abort_flag)) return false;
+        const int slot = j % C::NSLOT, bf = j % NBUF;
+        if (!mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t k_base = sbase + C::OFF_KV + sk * C::KV_BYTES;
-        const uint32_t v_base = sbase + C::OFF_KV + sv * C::KV_BYTES;
+        const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
+        const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * (QBM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_S + (j & 1) * QBN, sdesc_sw128(q_base + aoff, 16, 1024),
-                      sdesc_sw128(k_base + boff, 16, 1024), IDESC_S, kk > 0);
-          mma_bf16_ss(tmem + C::TM_DP + (j & 1) * QBN, sdesc_sw128(do_base + aoff, 16, 1024),
-                      sdesc_sw128(v_base + boff, 16, 1024), IDESC_S, kk > 0);
+          mma_bf16_ss(tmem + C::TM_S + bf * QBN, sdesc_add(q_desc, aoff), sdesc_add(k_desc, boff), IDESC_S, kk > 0);
         }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&kv_empty[sv]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (QBM * 128) + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TM_DP + bf * QBN, sdesc_add(do_desc, aoff), sdesc_add(v_desc, boff), IDESC_S, kk > 0);
+        }
+        mma_commit(&s_full[bf]);
         return true;
       };
       auto issue_dq = [&](int j) -> bool {
-        if (!mbar_wait(&ds_full[j & 1], (j >> 1) & 1, abort_flag)) return false;
+        const int slot = j % C::NSLOT, bf = j % NBUF;
+        if (!mbar_wait(&ds_full[bf], (j / NBUF) & 1, abort_flag)) return false;
         tc_fence_after();
-        const int sk = (2 * j) % C::NSLOT;
-        const uint32_t k_base = sbase + C::OFF_KV + sk * C::KV_BYTES;
+        const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < QBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + (j & 1) * QBN + kk * 8,
-                      sdesc_sw128(k_base + kk * 16 * 128, QBN * 128, 1024), IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&dq_done[j & 1]);
-        mma_commit(&kv_empty[sk]);
+          mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + kk * 8, sdesc_add(k_desc, kk * 16 * 128),
+                      IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&kv_empty[slot]);  // K_j, V_j no longer read
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok && n_kv > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < NBUF && j < n_kv; ++j) ok = issue_s(j);
       for (int j = 0; ok && j < n_kv; ++j) {
         ok = issue_dq(j);
-        if (ok && j + 2 < n_kv) ok = issue_s(j + 2);
+        if (ok && j + NBUF < n_kv) ok = issue_s(j + NBUF);
       }
+      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
@@ -340,8 +359,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(drain, 0, &never);
       }
     }
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;  // 0 or 1: key columns [32*wg, 32*wg + 32)
+  } else {
+    // ---------------------------------------------------------------- gradients (thread = row)
+    const int wg = (warp - 2) >> 2;
+    constexpr int NCOL = QBN / NWG;  // key columns of a tile this warpgroup forms
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int pos = p0 + r / p.G;
@@ -365,42 +386,47 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = warp_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag);
+      const int bf = j % NBUF;
+      ok = warp_wait(&s_full[bf], (j / NBUF) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[32], dpv[32];
-      tmem_ld32(tmem + lane_base + C::TM_S + (j & 1) * QBN + wg * 32, s);
-      tmem_ld32(tmem + lane_base + C::TM_DP + (j & 1) * QBN + wg * 32, dpv);
-      const int kb = j * QBN + wg * 32;
-      const int lim = valid ? pos - kb : -1;  // columns c <= lim are visible
-      uint32_t pk[16];
+      uint32_t pk[NCOL / 2];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float e0 = ex2(fmaf(__uint_as_float(s[c]), sl2, -lse2));
-        float e1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -lse2));
-        e0 = (c <= lim) ? e0 : 0.f;
-        e1 = (c + 1 <= lim) ? e1 : 0.f;
-        const float d0 = e0 * (__uint_as_float(dpv[c]) - dlt);
-        const float d1 = e1 * (__uint_as_float(dpv[c + 1]) - dlt);
-        pk[c >> 1] = pack_bf16(d0, d1);
+      for (int hf = 0; hf < NCOL / 32; ++hf) {
+        const int c0 = wg * NCOL + hf * 32;  // first key column of this group
+        uint32_t s[32], dpv[32];
+        tmem_ld32x2(tmem + lane_base + C::TM_S + bf * QBN + c0, tmem + lane_base + C::TM_DP + bf * QBN + c0, s, dpv);
+        const int lim = valid ? pos - (j * QBN + c0) : -1;  // columns c <= lim are visible
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float e0 = ex2(fmaf(__uint_as_float(s[c]), sl2, -lse2));
+          float e1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -lse2));
+          e0 = (c <= lim) ? e0 : 0.f;
+          e1 = (c + 1 <= lim) ? e1 : 0.f;
+          const float d0 = e0 * (__uint_as_float(dpv[c]) - dlt);
+          const float d1 = e1 * (__uint_as_float(dpv[c + 1]) - dlt);
+          pk[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
+        }
       }
-      // dS (bf16 pairs) into columns [16*wg, 16*wg+16) of S[j%2]
-      tmem_st16(tmem + lane_base + C::TM_S + (j & 1) * QBN + wg * 16, pk);
+      // dS (bf16 pairs) over the first 32 columns of S[bf]; this warpgroup's share
+      if constexpr (NCOL == 64)
+        tmem_st32(tmem + lane_base + C::TM_S + bf * QBN, pk);
+      else
+        tmem_st16(tmem + lane_base + C::TM_S + bf * QBN + wg * 16, pk);
       tc_fence_before();
-      mbar_arrive(&ds_full[j & 1]);
+      mbar_arrive(&ds_full[bf]);
     }
     if (!ok) {
       raise_abort(abort_flag, p.status);
     } else {
-      const int jl = n_kv - 1;
-      ok = warp_wait(&dq_done[jl & 1], (jl >> 1) & 1, abort_flag);
+      ok = warp_wait(last_done, 0, abort_flag);
       if (!ok) {
         raise_abort(abort_flag, p.status);
       } else {
         tc_fence_after();
-        // WG w writes dq columns [w*D/2, (w+1)*D/2)
+        // WG w writes dq columns [w*D/NWG, (w+1)*D/NWG)
 #pragma unroll 1
-        for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+        for (int c0 = wg * (D / NWG); c0 < (wg + 1) * (D / NWG); c0 += 32) {
           uint32_t acc[32];
           tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
           float extra[32];
@@ -442,22 +468,23 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TM_COLS);
   }
 }
 
 // ============================================================================ dK / dV
 // CTA: 128 keys [kb, kb+128) of (b, g).  Query tiles of 64 rows, head-major inside the
 // tile (row r -> head g*G + r/P', position p0 + r%P', P' = floor(64/G)), loaded by TMA
-// together with dO; their LSE (log2 units) and Delta are staged by the producer warp.
-// Warps: 0 TMA + row statistics, 1 MMA + TMEM, 4..11 two gradient warpgroups (WG w
-// handles query columns [32w, 32w+32)); thread = key (TMEM lane).
-// TMEM: S^T[2] cols [0,64) [64,128), dP^T[2] [128,192) [192,256), dV [256,256+d),
-// dK [256+d, 256+2d).  P^T and dS^T (bf16) overwrite the first 32 columns of their buffers.
+// together with dO; their LSE and Delta are copied asynchronously by the producer warp.
+// Warps: 0 loads, 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient warps (thread = key = TMEM
+// lane; with two warpgroups WG k handles query columns [32k, 32k+32), with one all 64).
+// TMEM: S^T[b] cols [64b, ..), dP^T[b] [64(NBUF+b), ..), dV [128 NBUF, +d), dK [+d, +2d).
+// P^T and dS^T (bf16) overwrite the first 32 columns of their buffers.
 constexpr int KBM = 128, KBN = 64;
 
-template <int D>
+template <int D, int NBUF, int NWG>
 struct DkvCfg {
+  static constexpr int THREADS = 64 + 128 * NWG;
   static constexpr int KV_BYTES = KBM * D * 2;   // the CTA's K (or V) tile
   static constexpr int QT_BYTES = KBN * D * 2;   // one 64-row Q (or dO) tile
   static constexpr int NSTAGE = 4;
@@ -467,19 +494,20 @@ struct DkvCfg {
   static constexpr int OFF_Q = 2 * KV_BYTES;     // stage s: Q at + s*STAGE, dO at + QT_BYTES
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][2][64] floats
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * 2 * KBN * 4;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], p_full[2], g_done[2], drain
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 7;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[NBUF], p_full[NBUF], drain, last_done
+  static constexpr int NBAR = 3 + 2 * NSTAGE + 2 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+  static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DV = 128 * NBUF, TM_DK = 128 * NBUF + D;
+  static constexpr uint32_t TM_COLS = (TM_DK + D) <= 256 ? 256 : 512;
 };
 
-template <int D>
-__global__ void __launch_bounds__(384, 1)
+template <int D, int NBUF, int NWG>
+__global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 1)
     moda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                          const BwdTcParams p) {
-  using C = DkvCfg<D>;
+  using C = DkvCfg<D, NBUF, NWG>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
@@ -488,7 +516,6 @@ __global__ void __launch_bounds__(384, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Pq = KBN / p.G;  // positions per query tile
-  const int n_kb = (p.T + KBM - 1) / KBM;
   const int ngroups = p.B * p.Hkv;
   const int kblk = static_cast<int>(blockIdx.x) / ngroups;  // smallest key blocks (most query tiles) first
   const int bg = static_cast<int>(blockIdx.x) % ngroups;
@@ -496,32 +523,31 @@ __global__ void __launch_bounds__(384, 1)
   const int kb = kblk * KBM;
   const int qt0 = kb / Pq, qt1 = (p.T - 1) / Pq;
   const int n_q = qt1 - qt0 + 1;
-  (void)n_kb;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NSTAGE;
   uint64_t* s_full = q_empty + C::NSTAGE;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* g_done = p_full + 2;
-  uint64_t* drain = g_done + 2;
+  uint64_t* p_full = s_full + NBUF;
+  uint64_t* drain = p_full + NBUF;
+  uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* stat = reinterpret_cast<float*>(smem + C::OFF_STAT);
+  const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT);
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int i = 0; i < C::NSTAGE; ++i) {
-      mbar_init(&q_full[i], 1);
+      mbar_init(&q_full[i], 1 + 32);  // TMA arrive + one cp.async arrival per producer lane
       mbar_init(&q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 256);
-      mbar_init(&g_done[i], 1);
+      mbar_init(&p_full[i], 128 * NWG);
     }
     mbar_init(drain, 1);
+    mbar_init(last_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -538,7 +564,7 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tmap(&tmO);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, C::TM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -565,18 +591,19 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       const int p0 = (qt0 + i) * Pq;
-      // row statistics of this tile: lse in log2 units (+inf for rows that do not exist), Delta
-      float* sl = stat + st * 2 * KBN;
+      // row statistics (LSE, Delta) of this tile, copied asynchronously.  Rows that do not
+      // exist (head >= G or position >= T) read a valid row's statistics: their Q and dO rows
+      // are zero in shared memory, so whatever finite P and dS they get contributes nothing.
+      const uint32_t sl = sbase + C::OFF_STAT + st * 2 * KBN * 4;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int r = lane + 32 * rr;
-        const int hh = r / Pq, pos = p0 + r % Pq;
-        const bool valid = hh < p.G && pos < p.T;
-        const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + (valid ? hh : 0)) * p.T + (valid ? pos : 0);
-        sl[r] = valid ? p.lse[row] * kLog2e : INFINITY;
-        sl[KBN + r] = valid ? p.delta[row] : 0.f;
+        const int hh = min(r / Pq, p.G - 1), pos = min(p0 + r % Pq, p.T - 1);
+        const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + pos;
+        cp_async_4(sl + r * 4, p.lse + row);
+        cp_async_4(sl + (KBN + r) * 4, p.delta + row);
       }
-      __syncwarp();
+      cp_async_arrive_noinc(&q_full[st]);
       if (lane == 0) {
         uint8_t* dst = smem + C::OFF_Q + st * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&q_full[st], static_cast<uint32_t>(2 * Pq * p.G * D * 2));
@@ -593,57 +620,66 @@ __global__ void __launch_bounds__(384, 1)
         raise_abort(abort_flag, p.status);
         volatile int never = 0;
         mbar_wait(kv_full, 0, &never);
-        for (int i = max(0, issued - C::NSTAGE); i < issued; ++i)
-          mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
       }
+      volatile int never = 0;
+      for (int i = max(0, issued - C::NSTAGE); i < issued; ++i)
+        mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(KBM, KBN, false);
       constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
-      const uint32_t k_base = sbase + C::OFF_K, v_base = sbase + C::OFF_V;
+      // descriptors built once; each MMA only advances the start address
+      const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t qt_desc_k = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);           // K-major Q/dO tiles
+      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, KBN * 128, 1024);   // MN-major Q/dO tiles
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       auto issue_s = [&](int i) -> bool {
-        const int st = i % C::NSTAGE;
+        const int st = i % C::NSTAGE, bf = i % NBUF;
         if (!mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t q_base = sbase + C::OFF_Q + st * C::STAGE_BYTES, o_base = q_base + C::QT_BYTES;
+        const uint64_t q_desc = sdesc_add(qt_desc_k, st * C::STAGE_BYTES);
+        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * (KBM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (KBN * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_S + (i & 1) * KBN, sdesc_sw128(k_base + aoff, 16, 1024),
-                      sdesc_sw128(q_base + boff, 16, 1024), IDESC_S, kk > 0);
-          mma_bf16_ss(tmem + C::TM_DP + (i & 1) * KBN, sdesc_sw128(v_base + aoff, 16, 1024),
-                      sdesc_sw128(o_base + boff, 16, 1024), IDESC_S, kk > 0);
+          mma_bf16_ss(tmem + C::TM_S + bf * KBN, sdesc_add(k_desc, aoff), sdesc_add(q_desc, boff), IDESC_S, kk > 0);
         }
-        mma_commit(&s_full[i & 1]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (KBM * 128) + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * (KBN * 128) + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::TM_DP + bf * KBN, sdesc_add(v_desc, aoff), sdesc_add(o_desc, boff), IDESC_S, kk > 0);
+        }
+        mma_commit(&s_full[bf]);
         return true;
       };
       auto issue_g = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag)) return false;
+        const int st = i % C::NSTAGE, bf = i % NBUF;
+        if (!mbar_wait(&p_full[bf], (i / NBUF) & 1, abort_flag)) return false;
         tc_fence_after();
-        const int st = i % C::NSTAGE;
-        const uint32_t q_base = sbase + C::OFF_Q + st * C::STAGE_BYTES, o_base = q_base + C::QT_BYTES;
+        const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
+        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < KBN / 16; ++kk) {
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + (i & 1) * KBN + kk * 8,
-                      sdesc_sw128(o_base + kk * 16 * 128, KBN * 128, 1024), IDESC_G, acc);
-          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + (i & 1) * KBN + kk * 8,
-                      sdesc_sw128(q_base + kk * 16 * 128, KBN * 128, 1024), IDESC_G, acc);
-        }
-        mma_commit(&g_done[i & 1]);
+        for (int kk = 0; kk < KBN / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + bf * KBN + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < KBN / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + bf * KBN + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
+                      (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&q_empty[st]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok && n_q > 1) ok = issue_s(1);
+      for (int i = 0; ok && i < NBUF && i < n_q; ++i) ok = issue_s(i);
       for (int i = 0; ok && i < n_q; ++i) {
         ok = issue_g(i);
-        if (ok && i + 2 < n_q) ok = issue_s(i + 2);
+        if (ok && i + NBUF < n_q) ok = issue_s(i + NBUF);
       }
+      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
@@ -651,70 +687,85 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(drain, 0, &never);
       }
     }
-  } else if (warp >= 4) {
+  } else {
     // ---------------------------------------------------------------- gradients (thread = key)
-    const int wg = (warp - 4) >> 2;
+    const int wg = (warp - 2) >> 2;
+    constexpr int NCOL = KBN / NWG;  // query columns of a tile this warpgroup forms
     const int kr = ((warp & 3) << 5) + lane;
     const int key = kb + kr;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
-      ok = warp_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag);
+      const int bf = i % NBUF;
+      ok = warp_wait(&s_full[bf], (i / NBUF) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[32], dpv[32];
-      tmem_ld32(tmem + lane_base + C::TM_S + (i & 1) * KBN + wg * 32, s);
-      tmem_ld32(tmem + lane_base + C::TM_DP + (i & 1) * KBN + wg * 32, dpv);
       const int st = i % C::NSTAGE;
-      const float* sl = stat + st * 2 * KBN + wg * 32;
+      const float* sl = stat + st * 2 * KBN;
       const int p0 = (qt0 + i) * Pq;
       const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
-      uint32_t pp[16], pd[16];
+      uint32_t pp[NCOL / 2], pd[NCOL / 2];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float e[2], dd[2];
+      for (int hf = 0; hf < NCOL / 32; ++hf) {
+        const int c0 = wg * NCOL + hf * 32;
+        uint32_t s[32], dpv[32];
+        tmem_ld32x2(tmem + lane_base + C::TM_S + bf * KBN + c0, tmem + lane_base + C::TM_DP + bf * KBN + c0, s, dpv);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int r = wg * 32 + c + u;
-          float x = ex2(fmaf(__uint_as_float(s[c + u]), sl2, -sl[c + u]));
-          if (diag && key > p0 + r % Pq) x = 0.f;
-          e[u] = x;
-          dd[u] = x * (__uint_as_float(dpv[c + u]) - sl[KBN + c + u]);
+        for (int c = 0; c < 32; c += 2) {
+          float e[2], dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int r = c0 + c + u;
+            float x = ex2(fmaf(__uint_as_float(s[c + u]), sl2, -sl[r] * kLog2e));
+            if (diag && key > p0 + r % Pq) x = 0.f;
+            e[u] = x;
+            dd[u] = x * (__uint_as_float(dpv[c + u]) - sl[KBN + r]);
+          }
+          pp[hf * 16 + (c >> 1)] = pack_bf16(e[0], e[1]);
+          pd[hf * 16 + (c >> 1)] = pack_bf16(dd[0], dd[1]);
         }
-        pp[c >> 1] = pack_bf16(e[0], e[1]);
-        pd[c >> 1] = pack_bf16(dd[0], dd[1]);
       }
-      tmem_st16(tmem + lane_base + C::TM_S + (i & 1) * KBN + wg * 16, pp);
-      tmem_st16(tmem + lane_base + C::TM_DP + (i & 1) * KBN + wg * 16, pd);
+      if constexpr (NCOL == 64) {
+        tmem_st32(tmem + lane_base + C::TM_S + bf * KBN, pp);
+        tmem_st32(tmem + lane_base + C::TM_DP + bf * KBN, pd);
+      } else {
+        tmem_st16(tmem + lane_base + C::TM_S + bf * KBN + wg * 16, pp);
+        tmem_st16(tmem + lane_base + C::TM_DP + bf * KBN + wg * 16, pd);
+      }
       tc_fence_before();
-      mbar_arrive(&p_full[i & 1]);
+      mbar_arrive(&p_full[bf]);
     }
     if (!ok) {
       raise_abort(abort_flag, p.status);
     } else {
-      const int il = n_q - 1;
-      ok = warp_wait(&g_done[il & 1], (il >> 1) & 1, abort_flag);
+      ok = warp_wait(last_done, 0, abort_flag);
       if (!ok) {
         raise_abort(abort_flag, p.status);
       } else {
         tc_fence_after();
-        // WG 0 writes dV, WG 1 writes dK (scaled)
-        const uint32_t src = wg == 0 ? C::TM_DV : C::TM_DK;
-        __nv_bfloat16* out = (wg == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
-        const float mul = wg == 0 ? 1.f : p.scale;
+        // dV (WG 0 / first half) and dK (scaled; WG 1 / second half)
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t acc[32];
-          tmem_ld32(tmem + lane_base + src + c0, acc);
-          if (key < p.T) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c0);
+        for (int part = 0; part < 2; ++part) {
+          if (NWG == 2 && part != wg) continue;
+          const uint32_t src = part == 0 ? C::TM_DV : C::TM_DK;
+          __nv_bfloat16* out =
+              (part == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
+          const float mul = part == 0 ? 1.f : p.scale;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t acc[32];
+            tmem_ld32(tmem + lane_base + src + c0, acc);
+            if (key < p.T) {
+              uint4* dst = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[u] = make_uint4(pack_bf16(__uint_as_float(acc[8 * u]) * mul, __uint_as_float(acc[8 * u + 1]) * mul),
-                                  pack_bf16(__uint_as_float(acc[8 * u + 2]) * mul, __uint_as_float(acc[8 * u + 3]) * mul),
-                                  pack_bf16(__uint_as_float(acc[8 * u + 4]) * mul, __uint_as_float(acc[8 * u + 5]) * mul),
-                                  pack_bf16(__uint_as_float(acc[8 * u + 6]) * mul, __uint_as_float(acc[8 * u + 7]) * mul));
+              for (int u = 0; u < 4; ++u)
+                dst[u] = make_uint4(
+                    pack_bf16(__uint_as_float(acc[8 * u]) * mul, __uint_as_float(acc[8 * u + 1]) * mul),
+                    pack_bf16(__uint_as_float(acc[8 * u + 2]) * mul, __uint_as_float(acc[8 * u + 3]) * mul),
+                    pack_bf16(__uint_as_float(acc[8 * u + 4]) * mul, __uint_as_float(acc[8 * u + 5]) * mul),
+                    pack_bf16(__uint_as_float(acc[8 * u + 6]) * mul, __uint_as_float(acc[8 * u + 7]) * mul));
+            }
           }
         }
       }
@@ -726,7 +777,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TM_COLS);
   }
 }
 
@@ -812,16 +863,21 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
       !make_map(&tk64, a.k, D, pr.T, planes_kv, QBN, 1) || !make_map(&tv64, a.v, D, pr.T, planes_kv, QBN, 1) ||
       !make_map(&tq, a.q, D, pr.T, planes_q, pq, pr.G) || !make_map(&to, a.dout, D, pr.T, planes_q, pq, pr.G))
     return cudaErrorInvalidValue;
+  // d = 64: single-buffered TMEM (256 columns), 192 threads, two CTAs per SM.
+  // d = 128: double-buffered TMEM, two gradient warpgroups, one CTA per SM.
+  constexpr int NBUF = D == 64 ? 1 : 2, NWG = D == 64 ? 1 : 2;
+  using KC = DkvCfg<D, NBUF, NWG>;
+  using QC = DqCfg<D, NBUF, NWG>;
   static int smem_dkdv = 0, smem_dq = 0;
-  e = set_smem(moda_bwd_dkdv_kernel<D>, DkvCfg<D>::SMEM, smem_dkdv);
+  e = set_smem(moda_bwd_dkdv_kernel<D, NBUF, NWG>, KC::SMEM, smem_dkdv);
   if (e != cudaSuccess) return e;
-  e = set_smem(moda_bwd_dq_kernel<D>, DqCfg<D>::SMEM, smem_dq);
+  e = set_smem(moda_bwd_dq_kernel<D, NBUF, NWG>, QC::SMEM, smem_dq);
   if (e != cudaSuccess) return e;
   const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
-  moda_bwd_dkdv_kernel<D><<<grid_kv, 384, DkvCfg<D>::SMEM, s>>>(tk128, tv128, tq, to, p);
+  moda_bwd_dkdv_kernel<D, NBUF, NWG><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
   const int P = QBM / pr.G;
   const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
-  moda_bwd_dq_kernel<D><<<grid_q, 384, DqCfg<D>::SMEM, s>>>(tk64, tv64, p);
+  moda_bwd_dq_kernel<D, NBUF, NWG><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
   count_launches(2);
   return cudaGetLastError();
 }

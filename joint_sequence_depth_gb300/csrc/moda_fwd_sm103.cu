@@ -209,19 +209,21 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
-      const uint32_t q_base = sbase + C::OFF_Q;
+      // descriptors built once; each MMA only advances the start address
+      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);          // K-major (K tiles)
+      const uint64_t kv_desc_v = sdesc_sw128(sbase + C::OFF_KV, BN * 128, 1024);    // MN-major (V tiles)
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto issue_s = [&](int j) -> bool {
         const int it = 2 * j, slot = it % C::NSLOT;
         if (!mbar_wait(&kv_full[slot], (it / C::NSLOT) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t k_base = sbase + C::OFF_KV + slot * C::KV_BYTES;
+        const uint64_t k_desc = sdesc_add(kv_desc_k, slot * C::KV_BYTES);
         const uint32_t d_tmem = tmem + C::TM_S0 + (j & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          mma_bf16_ss(d_tmem, sdesc_sw128(q_base + off, 16, 1024),
-                      sdesc_sw128(k_base + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024), IDESC_S, kk > 0);
+          mma_bf16_ss(d_tmem, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                      sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
         }
         mma_commit(&s_full[j & 1]);
         mma_commit(&kv_empty[slot]);
@@ -233,11 +235,11 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&kv_full[slot], (it / C::NSLOT) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t p_tmem = tmem + C::TM_S0 + (j & 1) * BN;
-        const uint32_t v_base = sbase + C::OFF_KV + slot * C::KV_BYTES;
+        const uint64_t v_desc = sdesc_add(kv_desc_v, slot * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_bf16_ts(tmem + C::TM_O, p_tmem + kk * 8, sdesc_sw128(v_base + kk * 16 * 128, BN * 128, 1024),
-                      IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::TM_O, p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&pv_done[j & 1]);
         mma_commit(&kv_empty[slot]);
