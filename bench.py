@@ -18,7 +18,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -41,6 +40,27 @@ def flops(shape):
     depth = 4.0 * B * H * T * S * d
     return {"fwd_seq": seq, "fwd_depth": depth, "fwd": seq + depth, "bwd_seq": 2.5 * seq,
             "bwd_depth": 2.5 * depth, "bwd": 2.5 * (seq + depth)}
+
+
+def kernel_counts(shape):
+    """Algorithmic FLOPs (tensor-core contractions over the causal triangle; one GEMM is
+    2*B*H*d*T(T+1)/2) and HBM bytes (each tensor read or written once) per launch of each
+    kernel of the step."""
+    e = 2 if shape.dtype_name == "bf16" else 4
+    B, H, Hkv, T, d, S = shape.B, shape.H, shape.Hkv, shape.T, shape.d, shape.S
+    gemm = 2.0 * B * H * d * T * (T + 1) / 2
+    q = B * H * T * d * e
+    kv = B * Hkv * T * d * e
+    dkv = B * Hkv * T * S * d * e
+    row = B * H * T * 4
+    qf32 = B * H * T * d * 4
+    return {
+        "moda_fwd_tc_kernel": {"flops": 2 * gemm, "bytes": q + 2 * kv + 2 * dkv + q + row},
+        "bwd_delta_kernel": {"flops": 0.0, "bytes": 2 * q + row},
+        "moda_bwd_depth_kernel": {"flops": 0.0, "bytes": 2 * dkv + 2 * q + 2 * row + 2 * dkv + qf32},
+        "moda_bwd_dkdv_kernel": {"flops": 4 * gemm, "bytes": 2 * kv + 2 * q + 2 * row + 2 * kv},
+        "moda_bwd_dq_kernel": {"flops": 3 * gemm, "bytes": 2 * q + 2 * kv + 2 * row + qf32 + q},
+    }
 
 
 def bytes_moved(shape):
@@ -83,7 +103,10 @@ def traffic_record(kernel, workload):
 
 
 KERNEL_SOURCES = {"moda_fwd_tc_kernel": ["moda_fwd_sm103.cu", "sm103_ptx.cuh"],
-                  "moda_bwd": ["moda_bwd_sm103.cu", "moda_simt.cu", "sm103_ptx.cuh"]}
+                  "bwd_delta_kernel": ["moda_simt.cu"],
+                  "moda_bwd_depth_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_bwd_dkdv_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_bwd_dq_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"]}
 
 
 def source_digest(kernel):
@@ -269,23 +292,30 @@ def main():
     if world > 1:
         dist.barrier()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    launches0 = binding.moda_launch_count()
+    # per step: start, after forward, after each backward stage (Delta, depth, dK/dV, dQ)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row_ev in ev:
+        for e_ in row_ev:
+            e_.record(stream)  # creates the event so its handle can be passed to the library
     torch.cuda.synchronize()
+    launches0 = binding.moda_launch_count()
     for i in range(K):
         ev[i][0].record(stream)
         binding.moda_fwd(q, k, v, kd, vd, o, lse)
         ev[i][1].record(stream)
-        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws)
-        ev[i][2].record(stream)
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:6])
     torch.cuda.synchronize()
     launches = binding.moda_launch_count() - launches0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][5])
     fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][5]) for i in range(K))
+    stage_names = ("moda_fwd_tc_kernel", "bwd_delta_kernel", "moda_bwd_depth_kernel", "moda_bwd_dkdv_kernel",
+                   "moda_bwd_dq_kernel")
+    kernel_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+                 for j, name in enumerate(stage_names)}
     status = binding.moda_device_status()
     if status != 0:
         raise RuntimeError(f"device status {binding.STATUS_NAMES.get(status, status)} after the timed steps")
@@ -328,28 +358,29 @@ def main():
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
     e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
 
-    # ------------------------------------------------------------- roofline of the dominant kernel
+    # ------------------------------------------------------------- roofline of each kernel
     peaks, peak_kind = load_peaks()
-    b = bytes_moved(shape)
-    if fwd_ms >= bwd_ms:
-        kernel, dur_ms, fl, by = "moda_fwd_tc_kernel", fwd_ms, f["fwd_seq"], b["fwd"]
-    else:
-        kernel, dur_ms, fl, by = "moda_bwd", bwd_ms, f["bwd_seq"], b["bwd"]
-    t_tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12)
-    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
-    if t_tensor >= t_hbm:
-        roof = {"bound": "tensor", "achieved": fl / (dur_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": by / (dur_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    counts = kernel_counts(shape)
+    kernels = {}
+    for name, ms in kernel_ms.items():
+        fl, by = counts[name]["flops"], counts[name]["bytes"]
+        t_tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+        if t_tensor >= t_hbm:
+            r = {"bound": "tensor", "achieved": fl / (ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops_sustained"],
+                 "unit": "TFLOP/s"}
+        else:
+            r = {"bound": "hbm", "achieved": by / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        r["frac"] = r["achieved"] / r["peak"]
+        r["ms"] = ms
+        r["algorithmic"] = {"flops": fl, "bytes": by}
+        kernels[name] = r
+    kernel = max(kernel_ms, key=kernel_ms.get)
+    roof = dict(kernels[kernel])
     roof["traffic"] = traffic_record(kernel, shape.name)
     roof["kernel"] = kernel
-    roof["algorithmic"] = {"flops": fl, "bytes": by}
     roof["peak_source"] = f"{peak_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'copy'})"
-    roof["step_share"] = dur_ms / (fwd_ms + bwd_ms)
-    roof["roofline_ms"] = max(t_tensor, t_hbm) * 1e3
-    roof["roofline_frac"] = max(t_tensor, t_hbm) * 1e3 / dur_ms
+    roof["step_share"] = kernel_ms[kernel] / (fwd_ms + bwd_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -365,7 +396,7 @@ def main():
                 "clocks": clk,
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": e2e_ms},
-                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu}
+                "gpu_launches": launches, "roofline": roof, "kernels": kernels, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -25,7 +25,8 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 # Names of every function include/moda.h declares.
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status", "moda_status_str",
-           "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes")
+           "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
+           "moda_bwd_profiled")
 
 
 class MODAError(RuntimeError):
@@ -58,6 +59,8 @@ def load_library():
             lib.moda_bwd_workspace_bytes.restype = ctypes.c_size_t
             lib.moda_bwd.argtypes = [d] + [p] * 14 + [ctypes.c_size_t, p]
             lib.moda_bwd.restype = ctypes.c_int
+            lib.moda_bwd_profiled.argtypes = [d] + [p] * 14 + [ctypes.c_size_t, p, ctypes.POINTER(p), ctypes.c_int32]
+            lib.moda_bwd_profiled.restype = ctypes.c_int
             lib.moda_device_status.argtypes = [ctypes.c_int, p]
             lib.moda_device_status.restype = ctypes.c_int
             lib.moda_status_str.argtypes = [ctypes.c_int]
@@ -130,8 +133,10 @@ def moda_bwd_workspace_bytes(desc: moda_desc) -> int:
     return int(load_library().moda_bwd_workspace_bytes(ctypes.byref(desc)))
 
 
-def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=None, stream=None):
-    """Backward of moda_fwd.  Returns (dq, dk, dv, dkd, dvd) in the input dtype."""
+def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=None, stream=None, events=None):
+    """Backward of moda_fwd.  Returns (dq, dk, dv, dkd, dvd) in the input dtype.  ``events``
+    (optional list of torch.cuda.Event) are recorded after each internal stage, see
+    moda_bwd_profiled in include/moda.h."""
     desc = _desc_from(q, k, kd, scale)
     if grads is None:
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
@@ -140,10 +145,15 @@ def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=No
     need = moda_bwd_workspace_bytes(desc)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = load_library().moda_bwd(
-        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None, _ptr(vd) if desc.S else None,
-        _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkd) if desc.S else None,
-        _ptr(dvd) if desc.S else None, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    args = (ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None,
+            _ptr(vd) if desc.S else None, _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(dkd) if desc.S else None, _ptr(dvd) if desc.S else None, _ptr(workspace),
+            ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if events is None:
+        st = load_library().moda_bwd(*args)
+    else:
+        handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        st = load_library().moda_bwd_profiled(*args, handles, len(events))
     if st != MODA_OK:
         raise MODAError(st, "moda_bwd")
     return dq, dk, dv, dkd, dvd

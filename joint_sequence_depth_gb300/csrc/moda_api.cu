@@ -138,6 +138,14 @@ size_t moda_bwd_workspace_bytes(const moda_desc* desc) {
 moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                      void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream) {
+  return moda_bwd_profiled(desc, q, k, v, kd, vd, o, lse, dout, dq, dk, dv, dkd, dvd, workspace, workspace_bytes,
+                           stream, nullptr, 0);
+}
+
+moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                              const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                              void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream,
+                              void** events, int32_t n_events) {
   moda_status st = check_desc(desc);
   if (st != MODA_OK) return st;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return MODA_ERR_INVALID_ARG;
@@ -165,6 +173,8 @@ moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const 
   a.dv = dv;
   a.dkd = desc->S > 0 ? dkd : nullptr;
   a.dvd = desc->S > 0 ? dvd : nullptr;
+  a.events = events;
+  a.n_events = events != nullptr ? n_events : 0;
   a.delta = static_cast<float*>(workspace);
   a.dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(desc));
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -39,7 +39,15 @@ struct BwdArgs {
   void *dq, *dk, *dv, *dkd, *dvd;
   float* delta;     // workspace [B,H,T]: D_t = dout_t . o_t
   float* dq_accum;  // workspace [B,H,T,d] float32 (tensor-core path)
+  void** events;    // optional cudaEvent_t[n_events]: events[k] recorded after the k-th kernel
+  int n_events;
 };
+
+// Records a.events[k] on `s` when the caller asked for it (profiling only).
+inline void mark_event(const BwdArgs& a, int k, cudaStream_t s) {
+  if (a.events != nullptr && k < a.n_events && a.events[k] != nullptr)
+    cudaEventRecord(static_cast<cudaEvent_t>(a.events[k]), s);
+}
 
 // Element loads/stores for the two storage types.
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -45,6 +45,8 @@ WORKLOADS = {
     "bf16_gqa": Shape("bf16_gqa", 4, 32, 8, 4096, 128, 24, torch.bfloat16),
     "bf16_long": Shape("bf16_long", 1, 32, 8, 16384, 128, 48, torch.bfloat16),
     "bf16_train": Shape("bf16_train", 8, 16, 4, 4096, 64, 32, torch.bfloat16, backward=True),
+    # a quarter of the training batch: the size kernel profiles are captured on
+    "bf16_train_quarter": Shape("bf16_train_quarter", 2, 16, 4, 4096, 64, 32, torch.bfloat16, backward=True),
 }
 
 # seed of each workload (its index in the list above, from 1)
