@@ -209,7 +209,7 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="bf16_train")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     return ap.parse_args()
 
 
@@ -292,8 +292,8 @@ def main():
     if world > 1:
         dist.barrier()
     K = args.steps
-    # per step: start, after forward, after each backward stage (Delta, depth, dK/dV, dQ)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    # per step: start, after forward, then start/end of each backward stage (Delta, depth, dK/dV, dQ)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(K)]
     for row_ev in ev:
         for e_ in row_ev:
             e_.record(stream)  # creates the event so its handle can be passed to the library
@@ -303,49 +303,84 @@ def main():
         ev[i][0].record(stream)
         binding.moda_fwd(q, k, v, kd, vd, o, lse)
         ev[i][1].record(stream)
-        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:6])
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:10])
     torch.cuda.synchronize()
     launches = binding.moda_launch_count() - launches0
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][5])
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][9])
     fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][5]) for i in range(K))
-    stage_names = ("moda_fwd_tc_kernel", "bwd_delta_kernel", "moda_bwd_depth_kernel", "moda_bwd_dkdv_kernel",
-                   "moda_bwd_dq_kernel")
-    kernel_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
-                 for j, name in enumerate(stage_names)}
+    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][9]) for i in range(K))
+    kernel_ms = {"moda_fwd_tc_kernel": fwd_ms}
+    for j, name in enumerate(("bwd_delta_kernel", "moda_bwd_depth_kernel", "moda_bwd_dkdv_kernel",
+                              "moda_bwd_dq_kernel")):
+        kernel_ms[name] = statistics.mean(ev[i][2 + 2 * j].elapsed_time(ev[i][3 + 2 * j]) for i in range(K))
     status = binding.moda_device_status()
     if status != 0:
         raise RuntimeError(f"device status {binding.STATUS_NAMES.get(status, status)} after the timed steps")
 
     # ------------------------------------------------------------- end to end (host buffers)
-    host_in = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "kd", "vd", "dout")}
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse) + grads]
-    dev_in = {"q": q, "k": k, "v": v, "kd": kd, "vd": vd, "dout": dout}
-    E = max(1, args.e2e_steps)
+    # Every step copies its inputs from pinned host memory, runs moda_fwd + moda_bwd and
+    # copies every output back to pinned host memory.  Steps are pipelined over two buffer
+    # sets: H2D of step i+1 and D2H of step i-1 run on their own streams while step i
+    # computes (the two copy directions use separate copy engines).
+    names = ("q", "k", "v", "kd", "vd", "dout")
+    host_in = {n: x[n].cpu().pin_memory() for n in names}
+    del x
+    sets = []
+    for _ in range(2):
+        din = {n: torch.empty_like(host_in[n], device=dev) for n in names}
+        dout_ = (torch.empty_like(din["q"]), torch.empty(base.B, base.H, base.T, dtype=torch.float32, device=dev),
+                 torch.empty_like(din["q"]), torch.empty_like(din["k"]), torch.empty_like(din["v"]),
+                 torch.empty_like(din["kd"]), torch.empty_like(din["vd"]))
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dout_]
+        sets.append((din, dout_, hout))
+    ws2 = torch.empty_like(ws)
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    E = max(3, args.e2e_steps)
 
-    def e2e_step():
-        for n, h in host_in.items():
-            dev_in[n].copy_(h, non_blocking=True)
-        step()
-        for h, d_ in zip(host_out, (o, lse) + grads):
-            h.copy_(d_, non_blocking=True)
+    def run_e2e(n_steps):
+        ev_h2d = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_d2h = [torch.cuda.Event() for _ in range(n_steps)]
+        for i in range(n_steps):
+            din, dout_, hout = sets[i % 2]
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(ev_comp[i - 2])  # set i%2 inputs no longer read
+                for n in names:
+                    din[n].copy_(host_in[n], non_blocking=True)
+                ev_h2d[i].record(h2d_s)
+            stream.wait_event(ev_h2d[i])
+            if i >= 2:
+                stream.wait_event(ev_d2h[i - 2])  # set i%2 outputs already copied out
+            o_, l_, *g_ = dout_
+            binding.moda_fwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_)
+            binding.moda_bwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_, din["dout"], tuple(g_),
+                             ws if i % 2 == 0 else ws2)
+            ev_comp[i].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_comp[i])
+                for h, d_ in zip(hout, dout_):
+                    h.copy_(d_, non_blocking=True)
+                ev_d2h[i].record(d2h_s)
+        return ev_d2h[-1]
 
-    e2e_step()
+    run_e2e(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(E):
-        e2e_step()
+    h2d_s.wait_event(e0)
+    last = run_e2e(E)
+    stream.wait_event(last)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / E
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
 
     if world > 1:
         t = torch.tensor([total_ms, e2e_ms, fwd_ms, bwd_ms], device=dev)
@@ -380,7 +415,7 @@ def main():
     roof["traffic"] = traffic_record(kernel, shape.name)
     roof["kernel"] = kernel
     roof["peak_source"] = f"{peak_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'copy'})"
-    roof["step_share"] = kernel_ms[kernel] / (fwd_ms + bwd_ms)
+    roof["step_share"] = kernel_ms[kernel] / ms_per_step
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

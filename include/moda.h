@@ -99,9 +99,10 @@ moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const 
 
 /* moda_bwd with timing marks for profilers and benchmarks: same arguments, kernels and
  * results, plus `events`, an array of n_events cudaEvent_t handles (created by the
- * caller; entries may be NULL).  events[k] is recorded on `stream` right after the
- * k-th stage: 0 = row statistics (Delta), 1 = depth-slot gradients, 2 = dK/dV,
- * 3 = dQ.  Events beyond n_events are not recorded. */
+ * caller; entries may be NULL).  Stage k is bracketed by events[2k] (start) and
+ * events[2k+1] (end), recorded on the stream that runs it: 0 = row statistics (Delta),
+ * 1 = depth-slot gradients, 2 = dK/dV, 3 = dQ.  Events beyond n_events are not recorded.
+ */
 moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                               const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                               void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream,

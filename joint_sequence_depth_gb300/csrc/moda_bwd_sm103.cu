@@ -845,10 +845,14 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.dvd = static_cast<__nv_bfloat16*>(a.dvd);
   p.status = a.status;
 
+  // stage 0: Delta; stage 1: depth gradients; stage 2: dK/dV; stage 3: dQ (needs stage 1's
+  // depth share of dQ).
+  mark_event(a, 0, s);
   cudaError_t e = launch_bwd_delta(a, 1, s);
   if (e != cudaSuccess) return e;
-  mark_event(a, 0, s);
+  mark_event(a, 1, s);
   const int64_t positions = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;
+  mark_event(a, 2, s);
   if (pr.S > 0) {
     const unsigned grid = static_cast<unsigned>((positions + 7) / 8);
     if (pr.G == 1) moda_bwd_depth_kernel<D, 1><<<grid, 256, 0, s>>>(p);
@@ -857,7 +861,7 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     else moda_bwd_depth_kernel<D, 8><<<grid, 256, 0, s>>>(p);
     count_launches(1);
   }
-  mark_event(a, 1, s);
+  mark_event(a, 3, s);
   CUtensorMap tk128, tv128, tk64, tv64, tq, to;
   const int planes_kv = pr.B * pr.Hkv, planes_q = pr.B * pr.H;
   const int pq = KBN / pr.G;
@@ -876,12 +880,14 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   e = set_smem(moda_bwd_dq_kernel<D, NBUF, NWG>, QC::SMEM, smem_dq);
   if (e != cudaSuccess) return e;
   const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
+  mark_event(a, 4, s);
   moda_bwd_dkdv_kernel<D, NBUF, NWG><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
-  mark_event(a, 2, s);
+  mark_event(a, 5, s);
   const int P = QBM / pr.G;
   const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
+  mark_event(a, 6, s);
   moda_bwd_dq_kernel<D, NBUF, NWG><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
-  mark_event(a, 3, s);
+  mark_event(a, 7, s);
   count_launches(2);
   return cudaGetLastError();
 }

@@ -39,7 +39,7 @@ struct BwdArgs {
   void *dq, *dk, *dv, *dkd, *dvd;
   float* delta;     // workspace [B,H,T]: D_t = dout_t . o_t
   float* dq_accum;  // workspace [B,H,T,d] float32 (tensor-core path)
-  void** events;    // optional cudaEvent_t[n_events]: events[k] recorded after the k-th kernel
+  void** events;    // optional cudaEvent_t[n_events]: stage k recorded at events[2k] (start), [2k+1] (end)
   int n_events;
 };
 

@@ -283,16 +283,20 @@ cudaError_t fwd_simt(const FwdArgs& a, cudaStream_t s) {
 template <typename T, int D>
 cudaError_t bwd_simt(const BwdArgs& a, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.p.B) * a.p.H * a.p.T;
-  bwd_delta_kernel<T, D><<<static_cast<unsigned>((rows + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
   mark_event(a, 0, s);
+  bwd_delta_kernel<T, D><<<static_cast<unsigned>((rows + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
+  mark_event(a, 1, s);
+  mark_event(a, 2, s);
   if (a.p.S > 0)
     bwd_depth_simt_kernel<T, D>
         <<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
-  mark_event(a, 1, s);
-  bwd_dkdv_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
-  mark_event(a, 2, s);
-  bwd_dq_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.H, a.p.T), kWarps * 32, 0, s>>>(a);
   mark_event(a, 3, s);
+  mark_event(a, 4, s);
+  bwd_dkdv_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
+  mark_event(a, 5, s);
+  mark_event(a, 6, s);
+  bwd_dq_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.H, a.p.T), kWarps * 32, 0, s>>>(a);
+  mark_event(a, 7, s);
   count_launches(a.p.S > 0 ? 4 : 3);
   return cudaGetLastError();
 }
