@@ -93,7 +93,7 @@ moda_status finish(cudaError_t launch, cudaStream_t s) {
 
 size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-size_t delta_bytes(const moda_desc* d) { return align256(size_t(d->B) * d->H * d->T * sizeof(float)); }
+size_t stats_bytes(const moda_desc* d) { return align256(size_t(d->B) * d->H * d->T * 2 * sizeof(float)); }
 size_t dq_accum_bytes(const moda_desc* d) {
   return align256(size_t(d->B) * d->H * d->T * d->d * sizeof(float));
 }
@@ -132,7 +132,7 @@ moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const 
 
 size_t moda_bwd_workspace_bytes(const moda_desc* desc) {
   if (check_desc(desc) != MODA_OK) return 0;
-  return delta_bytes(desc) + dq_accum_bytes(desc);
+  return stats_bytes(desc) + dq_accum_bytes(desc);
 }
 
 moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
@@ -175,8 +175,8 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
   a.dvd = desc->S > 0 ? dvd : nullptr;
   a.events = events;
   a.n_events = events != nullptr ? n_events : 0;
-  a.delta = static_cast<float*>(workspace);
-  a.dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(desc));
+  a.stats = static_cast<float2*>(workspace);
+  a.dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + stats_bytes(desc));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (desc->dtype == MODA_DTYPE_BF16 && moda::bwd_sm103_supported(a.p))

@@ -44,7 +44,7 @@ struct BwdTcParams {
   float scale, scale_log2;
   const __nv_bfloat16 *q, *k, *v, *kd, *vd, *dout;
   const float* lse;
-  const float* delta;
+  const float2* stats;  // {-lse * log2(e), Delta} per row
   float* dq_accum;  // depth share of dq, float32 [B,H,T,d] (read by the dQ kernel when S > 0)
   __nv_bfloat16 *dq, *dk, *dv, *dkd, *dvd;
   int* status;
@@ -76,8 +76,9 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
     const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + (hv ? hh : 0)) * p.T + t;
     qv[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.q + row * D) + cc) : make_uint4(0, 0, 0, 0);
     dv4[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.dout + row * D) + cc) : make_uint4(0, 0, 0, 0);
-    lse2[hh] = hv ? p.lse[row] * kLog2e : INFINITY;
-    dl[hh] = hv ? p.delta[row] : 0.f;
+    const float2 st = hv ? p.stats[row] : make_float2(-INFINITY, 0.f);
+    lse2[hh] = -st.x;
+    dl[hh] = st.y;
 #pragma unroll
     for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
   }
@@ -381,8 +382,9 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
       fence_proxy_async_smem();
       mbar_arrive(q_full);
     }
-    const float lse2 = valid ? p.lse[row] * kLog2e : INFINITY;
-    const float dlt = valid ? p.delta[row] : 0.f;
+    const float2 st = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
+    const float nlse2 = st.x;  // -lse * log2(e)
+    const float dlt = st.y;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -397,14 +399,21 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
         uint32_t s[32], dpv[32];
         tmem_ld32x2(tmem + lane_base + C::TM_S + bf * QBN + c0, tmem + lane_base + C::TM_DP + bf * QBN + c0, s, dpv);
         const int lim = valid ? pos - (j * QBN + c0) : -1;  // columns c <= lim are visible
+        float e[32];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float e0 = ex2(fmaf(__uint_as_float(s[c]), sl2, -lse2));
-          float e1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -lse2));
-          e0 = (c <= lim) ? e0 : 0.f;
-          e1 = (c + 1 <= lim) ? e1 : 0.f;
-          const float d0 = e0 * (__uint_as_float(dpv[c]) - dlt);
-          const float d1 = e1 * (__uint_as_float(dpv[c + 1]) - dlt);
+          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
+          e[c] = ex2(e[c]);
+          e[c + 1] = ex2(e[c + 1]);
+        }
+        if (lim < 31) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float d0, d1;
+          fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, dlt, e[c], e[c + 1], d0, d1);
           pk[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
         }
       }
@@ -492,7 +501,7 @@ struct DkvCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_BYTES;
   static constexpr int OFF_Q = 2 * KV_BYTES;     // stage s: Q at + s*STAGE, dO at + QT_BYTES
-  static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][2][64] floats
+  static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][64] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * 2 * KBN * 4;
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[NBUF], p_full[NBUF], drain, last_done
   static constexpr int NBAR = 3 + 2 * NSTAGE + 2 * NBUF;
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  const float* stat = reinterpret_cast<const float*>(smem + C::OFF_STAT);
+  const float4* stat = reinterpret_cast<const float4*>(smem + C::OFF_STAT);  // two rows per float4
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -594,14 +603,13 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       // row statistics (LSE, Delta) of this tile, copied asynchronously.  Rows that do not
       // exist (head >= G or position >= T) read a valid row's statistics: their Q and dO rows
       // are zero in shared memory, so whatever finite P and dS they get contributes nothing.
-      const uint32_t sl = sbase + C::OFF_STAT + st * 2 * KBN * 4;
+      const uint32_t sl = sbase + C::OFF_STAT + st * KBN * 8;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int r = lane + 32 * rr;
         const int hh = min(r / Pq, p.G - 1), pos = min(p0 + r % Pq, p.T - 1);
         const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + pos;
-        cp_async_4(sl + r * 4, p.lse + row);
-        cp_async_4(sl + (KBN + r) * 4, p.delta + row);
+        cp_async_8(sl + r * 8, p.stats + row);
       }
       cp_async_arrive_noinc(&q_full[st]);
       if (lane == 0) {
@@ -702,7 +710,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       if (!ok) break;
       tc_fence_after();
       const int st = i % C::NSTAGE;
-      const float* sl = stat + st * 2 * KBN;
+      const float4* sl = stat + st * (KBN / 2);
       const int p0 = (qt0 + i) * Pq;
       const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
       uint32_t pp[NCOL / 2], pd[NCOL / 2];
@@ -711,19 +719,32 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
         const int c0 = wg * NCOL + hf * 32;
         uint32_t s[32], dpv[32];
         tmem_ld32x2(tmem + lane_base + C::TM_S + bf * KBN + c0, tmem + lane_base + C::TM_DP + bf * KBN + c0, s, dpv);
+        float e[32];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float e[2], dd[2];
+          const float4 rs = sl[(c0 + c) >> 1];  // rows c0+c, c0+c+1: {-lse2, Delta, -lse2, Delta}
+          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, rs.x, rs.z, e[c], e[c + 1]);
+          e[c] = ex2(e[c]);
+          e[c + 1] = ex2(e[c + 1]);
+        }
+        if (diag) {
+          // row r sits at position p0 + r % Pq (head-major tile); keys after it are masked
+          const int dk = key - p0;
+          if ((Pq & (Pq - 1)) == 0) {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = c0 + c + u;
-            float x = ex2(fmaf(__uint_as_float(s[c + u]), sl2, -sl[r] * kLog2e));
-            if (diag && key > p0 + r % Pq) x = 0.f;
-            e[u] = x;
-            dd[u] = x * (__uint_as_float(dpv[c + u]) - sl[KBN + r]);
+            for (int c = 0; c < 32; ++c) e[c] = (dk > ((c0 + c) & (Pq - 1))) ? 0.f : e[c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) e[c] = (dk > (c0 + c) % Pq) ? 0.f : e[c];
           }
-          pp[hf * 16 + (c >> 1)] = pack_bf16(e[0], e[1]);
-          pd[hf * 16 + (c >> 1)] = pack_bf16(dd[0], dd[1]);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float4 rs = sl[(c0 + c) >> 1];
+          float d0, d1;
+          fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), rs.y, rs.w, e[c], e[c + 1], d0, d1);
+          pp[hf * 16 + (c >> 1)] = pack_bf16(e[c], e[c + 1]);
+          pd[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
         }
       }
       if constexpr (NCOL == 64) {
@@ -836,7 +857,7 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.vd = static_cast<const __nv_bfloat16*>(a.vd);
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.lse = a.lse;
-  p.delta = a.delta;
+  p.stats = a.stats;
   p.dq_accum = a.dq_accum;
   p.dq = static_cast<__nv_bfloat16*>(a.dq);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);

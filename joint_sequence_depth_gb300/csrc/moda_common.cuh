@@ -37,7 +37,7 @@ struct BwdArgs {
   const void *q, *k, *v, *kd, *vd, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv, *dkd, *dvd;
-  float* delta;     // workspace [B,H,T]: D_t = dout_t . o_t
+  float2* stats;    // workspace [B,H,T]: {-lse * log2(e), Delta_t = dout_t . o_t}
   float* dq_accum;  // workspace [B,H,T,d] float32 (tensor-core path)
   void** events;    // optional cudaEvent_t[n_events]: stage k recorded at events[2k] (start), [2k+1] (end)
   int n_events;

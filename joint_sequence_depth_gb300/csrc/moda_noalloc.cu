@@ -24,8 +24,8 @@
 
 namespace {
 
-// 32 MiB: enough for problems with B*H*T*(d+1)*4 bytes of workspace up to this size
-// (for example B*H*T = 126,000 rows at d = 64, or 64,000 rows at d = 128).
+// 32 MiB: enough for problems with B*H*T*(d+2)*4 bytes of workspace up to this size
+// (for example B*H*T = 127,000 rows at d = 64, or 64,000 rows at d = 128).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const FwdArgs a) 
 }
 
 // ---------------------------------------------------------------- backward
-// D_t = dout_t . o_t for every row (b, h, t).
+// Row statistics for every row (b, h, t): {-lse * log2(e), Delta_t = dout_t . o_t}.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) bwd_delta_kernel(const BwdArgs a) {
   constexpr int N = D / 32;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_delta_kernel(const BwdArgs a)
   load_frag(static_cast<const T*>(a.o) + row * D + lane * N, of);
   load_frag(static_cast<const T*>(a.dout) + row * D + lane * N, df);
   const float s = warp_sum(dot(of, df));
-  if (lane == 0) a.delta[row] = s;
+  if (lane == 0) a.stats[row] = make_float2(-a.lse[row] * kLog2e, s);
 }
 
 // dq for one row: sequence keys j <= t, then the depth slots of position t.
@@ -168,8 +168,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(const BwdArgs 
     qf[c] *= p.scale_log2;
     dq[c] = 0.f;
   }
-  const float lse2 = a.lse[row] * kLog2e;
-  const float Dt = a.delta[row];
+  const float2 st = a.stats[row];
+  const float lse2 = -st.x;
+  const float Dt = st.y;
   for (int j = 0; j <= t; ++j) {
     load_frag(k + static_cast<int64_t>(j) * D, kf);
     load_frag(v + static_cast<int64_t>(j) * D, vf);
@@ -218,8 +219,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(const BwdArg
       const int64_t row = bh * p.T + t;
       load_frag(static_cast<const T*>(a.q) + row * D + lane * N, qf);
       load_frag(static_cast<const T*>(a.dout) + row * D + lane * N, df);
-      const float pj = exp2f(warp_sum(dot(qf, kf)) * p.scale_log2 - a.lse[row] * kLog2e);
-      const float ds = pj * (warp_sum(dot(df, vf)) - a.delta[row]);
+      const float2 st = a.stats[row];
+      const float pj = exp2f(warp_sum(dot(qf, kf)) * p.scale_log2 + st.x);
+      const float ds = pj * (warp_sum(dot(df, vf)) - st.y);
 #pragma unroll
       for (int c = 0; c < N; ++c) {
         dk[c] = fmaf(ds, qf[c], dk[c]);
@@ -255,8 +257,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_depth_simt_kernel(const BwdAr
       const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + t;
       load_frag(static_cast<const T*>(a.q) + row * D + lane * N, qf);
       load_frag(static_cast<const T*>(a.dout) + row * D + lane * N, df);
-      const float pj = exp2f(warp_sum(dot(qf, kf)) * p.scale_log2 - a.lse[row] * kLog2e);
-      const float ds = pj * (warp_sum(dot(df, vf)) - a.delta[row]);
+      const float2 st = a.stats[row];
+      const float pj = exp2f(warp_sum(dot(qf, kf)) * p.scale_log2 + st.x);
+      const float ds = pj * (warp_sum(dot(df, vf)) - st.y);
 #pragma unroll
       for (int c = 0; c < N; ++c) {
         dk[c] = fmaf(ds, qf[c], dk[c]);

@@ -258,6 +258,39 @@ __device__ __forceinline__ void ffma2_bc(float a0, float a1, float b, float c, f
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1) as one packed fp32x2 FMA.
+__device__ __forceinline__ void ffma2(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
+                                      float& d1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 x, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) = ((a0, a1) - (b0, b1)) * (c0, c1): packed subtract then packed multiply.
+__device__ __forceinline__ void fsubmul2(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
+                                         float& d1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%6, %7};\n\t"
+      "sub.rn.f32x2 x, x, y;\n\t"
+      "mul.rn.f32x2 x, x, z;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// 8-byte asynchronous global -> shared copy (see cp_async_4).
+__device__ __forceinline__ void cp_async_8(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
 // (a0, a1) += (b0, b1) as one packed fp32x2 add.
 __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
   asm("{\n\t.reg .b64 x, y;\n\t"
