@@ -748,8 +748,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
         }
       }
       if constexpr (NCOL == 64) {
-        tmem_st32(tmem + lane_base + C::TM_S + bf * KBN, pp);
-        tmem_st32(tmem + lane_base + C::TM_DP + bf * KBN, pd);
+        tmem_st32x2(tmem + lane_base + C::TM_S + bf * KBN, tmem + lane_base + C::TM_DP + bf * KBN, pp, pd);
       } else {
         tmem_st16(tmem + lane_base + C::TM_S + bf * KBN + wg * 16, pp);
         tmem_st16(tmem + lane_base + C::TM_DP + bf * KBN + wg * 16, pd);
@@ -892,22 +891,23 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   // d = 64: single-buffered TMEM (256 columns), 192 threads, two CTAs per SM.
   // d = 128: double-buffered TMEM, two gradient warpgroups, one CTA per SM.
-  constexpr int NBUF = D == 64 ? 1 : 2, NWG = D == 64 ? 1 : 2;
-  using KC = DkvCfg<D, NBUF, NWG>;
-  using QC = DqCfg<D, NBUF, NWG>;
+  constexpr int KNB = D == 64 ? 1 : 2, KNW = KNB;
+  constexpr int QNB = D == 64 ? 1 : 2, QNW = QNB;
+  using KC = DkvCfg<D, KNB, KNW>;
+  using QC = DqCfg<D, QNB, QNW>;
   static int smem_dkdv = 0, smem_dq = 0;
-  e = set_smem(moda_bwd_dkdv_kernel<D, NBUF, NWG>, KC::SMEM, smem_dkdv);
+  e = set_smem(moda_bwd_dkdv_kernel<D, KNB, KNW>, KC::SMEM, smem_dkdv);
   if (e != cudaSuccess) return e;
-  e = set_smem(moda_bwd_dq_kernel<D, NBUF, NWG>, QC::SMEM, smem_dq);
+  e = set_smem(moda_bwd_dq_kernel<D, QNB, QNW>, QC::SMEM, smem_dq);
   if (e != cudaSuccess) return e;
   const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
   mark_event(a, 4, s);
-  moda_bwd_dkdv_kernel<D, NBUF, NWG><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
+  moda_bwd_dkdv_kernel<D, KNB, KNW><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
   mark_event(a, 5, s);
   const int P = QBM / pr.G;
   const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
   mark_event(a, 6, s);
-  moda_bwd_dq_kernel<D, NBUF, NWG><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
+  moda_bwd_dq_kernel<D, QNB, QNW><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
   mark_event(a, 7, s);
   count_launches(2);
   return cudaGetLastError();
