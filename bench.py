@@ -220,6 +220,30 @@ def dist_setup(args):
     return world, rank, local
 
 
+def rank_seed(workload, rank):
+    """Each rank draws its own batch: replicas work on independent problems."""
+    from joint_sequence_depth_gb300.inputs import SEEDS
+
+    return SEEDS[workload] + 1000 * rank
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum over all ranks (the slowest rank sets every time)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_tflops(step_flops, ms_per_step, world):
+    """Whole-job throughput: every rank processed step_flops per step in ms_per_step."""
+    return world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+
 def run_reference(args, shape):
     world, rank, _ = dist_setup(args)
     if rank != 0:
@@ -248,7 +272,7 @@ def workload_config(shape):
 
 def main():
     args = parse()
-    from joint_sequence_depth_gb300.inputs import SEEDS, WORKLOADS
+    from joint_sequence_depth_gb300.inputs import WORKLOADS
 
     base = WORKLOADS[args.workload]
     shape = base
@@ -270,7 +294,7 @@ def main():
     mbuild.build()
     binding.load_library()
 
-    x = make_inputs(base, seed=SEEDS[args.workload] + 1000 * rank, device=dev, with_dout=True)
+    x = make_inputs(base, seed=rank_seed(args.workload, rank), device=dev, with_dout=True)
     q, k, v, kd, vd, dout = (x[n] for n in ("q", "k", "v", "kd", "vd", "dout"))
     o = torch.empty_like(q)
     lse = torch.empty(base.B, base.H, base.T, dtype=torch.float32, device=dev)
@@ -382,16 +406,13 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms, fwd_ms, bwd_ms = t.tolist()
+    total_ms, e2e_ms, fwd_ms, bwd_ms = max_over_ranks([total_ms, e2e_ms, fwd_ms, bwd_ms], dev)
 
     f = flops(shape)
     step_flops = f["fwd"] + f["bwd"]
     ms_per_step = total_ms / K
-    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
-    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+    value = aggregate_tflops(step_flops, ms_per_step, world)
+    e2e_value = aggregate_tflops(step_flops, e2e_ms, world)
 
     # ------------------------------------------------------------- roofline of each kernel
     peaks, peak_kind = load_peaks()

@@ -133,6 +133,17 @@ moda_status moda_device_status(int clear, void* stream);
 /* Human-readable name of a status code (static storage). */
 const char* moda_status_str(moda_status status);
 
+/* Self-test of the device-side failure path (no counterpart in the paper: it exists
+ * so the timeout handling can be tested without hanging or faulting a GPU).
+ * Launches one CTA whose first warp waits on an mbarrier that no thread arrives at
+ * for at most limit_ns nanoseconds (clamped to [1e6, 2e9]) and then raises the CTA's
+ * abort flag; its second warp waits on the same barrier and must leave on that flag,
+ * long before the 2 s cap every kernel wait has.  Waits for `stream`, then returns
+ * the status word and clears it: MODA_ERR_TIMEOUT when both waits gave up the
+ * designed way, MODA_ERR_CUDA if either did not or a CUDA call failed.  A status
+ * left by an earlier call is cleared first.  The context stays usable. */
+moda_status moda_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t moda_version(void);
 

@@ -26,7 +26,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 # Names of every function include/moda.h declares.
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status", "moda_status_str",
            "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
-           "moda_bwd_profiled")
+           "moda_bwd_profiled", "moda_selftest_wait_timeout")
 
 
 class MODAError(RuntimeError):
@@ -73,6 +73,8 @@ def load_library():
             lib.moda_bwd_noalloc.restype = ctypes.c_int
             lib.moda_bwd_noalloc_max_workspace_bytes.argtypes = []
             lib.moda_bwd_noalloc_max_workspace_bytes.restype = ctypes.c_size_t
+            lib.moda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, p]
+            lib.moda_selftest_wait_timeout.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -161,6 +163,12 @@ def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=No
 
 def moda_device_status(clear=True, stream=None) -> int:
     return int(load_library().moda_device_status(1 if clear else 0, _stream(stream)))
+
+
+def moda_selftest_wait_timeout(limit_ns=20_000_000, stream=None) -> int:
+    """Runs the bounded-wait self-test kernel on the current device; returns the status
+    it produced (MODA_ERR_TIMEOUT = 4 when the failure path worked)."""
+    return int(load_library().moda_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def moda_launch_count() -> int:

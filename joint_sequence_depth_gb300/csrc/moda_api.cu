@@ -186,6 +186,18 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
   return finish(e, s);
 }
 
+moda_status moda_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* w = status_word();
+  if (w == nullptr) return MODA_ERR_CUDA;
+  // leave no earlier error behind that would mask the result
+  moda_status before = read_status(1, s);
+  if (before == MODA_ERR_CUDA) return MODA_ERR_CUDA;
+  const uint64_t lim = limit_ns < 1000000ull ? 1000000ull : (limit_ns > 2000000000ull ? 2000000000ull : limit_ns);
+  if (moda::launch_wait_selftest(w, lim, s) != cudaSuccess) return MODA_ERR_CUDA;
+  return read_status(1, s);
+}
+
 moda_status moda_device_status(int clear, void* stream) {
   return read_status(clear, static_cast<cudaStream_t>(stream));
 }

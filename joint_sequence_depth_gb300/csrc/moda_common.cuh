@@ -69,6 +69,7 @@ void count_launches(int n);
 cudaError_t launch_fwd_simt(const FwdArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, cudaStream_t s);  // Delta = rowsum(dout * o)
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s);
 bool fwd_sm103_supported(const Problem& p);
