@@ -82,6 +82,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -260,6 +269,33 @@ __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, ui
       : "memory");
 }
 
+// L2 policy for data read exactly once (streamed depth slabs): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_load with an L2 cache policy (see l2_policy_evict_first).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst_smem, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst_smem),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Register reallocation between warpgroups (all warps of a warpgroup execute the same one).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 4-byte asynchronous global -> shared copy; completion is tracked by the mbarrier
 // named in a later cp_async_arrive_noinc by the same thread.
 __device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src) {
@@ -389,6 +425,36 @@ __device__ __forceinline__ void axpy2_bf16(uint32_t p16, uint32_t v, float& a0, 
       "fma.rn.f32.bf16 %1, pl, vh, %1;\n\t}"
       : "+f"(a0), "+f"(a1)
       : "r"(p16), "r"(v));
+}
+
+// (a0, a1) += p * (v.lo, v.hi), p a bf16 in the high half of `p16`.
+__device__ __forceinline__ void axpy2_bf16_hi(uint32_t p16, uint32_t v, float& a0, float& a1) {
+  asm("{\n\t.reg .b16 pl, ph, vl, vh;\n\t"
+      "mov.b32 {pl, ph}, %2;\n\t"
+      "mov.b32 {vl, vh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, ph, vl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ph, vh, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(p16), "r"(v));
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
