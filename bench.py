@@ -302,11 +302,10 @@ def main():
              torch.empty_like(vd))
     desc = binding.make_desc(base.B, base.H, base.Hkv, base.T, base.S, base.d, base.dtype)
     ws = torch.empty(binding.moda_bwd_workspace_bytes(desc), dtype=torch.uint8, device=dev)
-    ws_f = torch.empty(max(256, binding.moda_fwd_workspace_bytes(desc)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        binding.moda_fwd(q, k, v, kd, vd, o, lse, workspace=ws_f)
+        binding.moda_fwd(q, k, v, kd, vd, o, lse)
         binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws)
 
     clocks = ClockSampler(local)
@@ -326,7 +325,7 @@ def main():
     launches0 = binding.moda_launch_count()
     for i in range(K):
         ev[i][0].record(stream)
-        binding.moda_fwd(q, k, v, kd, vd, o, lse, workspace=ws_f)
+        binding.moda_fwd(q, k, v, kd, vd, o, lse)
         ev[i][1].record(stream)
         binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:10])
     torch.cuda.synchronize()
@@ -381,7 +380,7 @@ def main():
             if i >= 2:
                 stream.wait_event(ev_d2h[i - 2])  # set i%2 outputs already copied out
             o_, l_, *g_ = dout_
-            binding.moda_fwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_, workspace=ws_f)
+            binding.moda_fwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_)
             binding.moda_bwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_, din["dout"], tuple(g_),
                              ws if i % 2 == 0 else ws2)
             ev_comp[i].record(stream)

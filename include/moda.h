@@ -70,25 +70,15 @@ typedef struct {
   float scale;
 } moda_desc;
 
-/* Device workspace bytes moda_fwd needs for this description on the CURRENT
- * device (the tensor-core path keeps per-CTA partial depth states, 2*256*(d+2)
- * float32 per persistent CTA, in it; the number of CTAs follows the device's SM
- * count).  0 for an invalid description and when no workspace is needed
- * (float32, S == 0, or shapes served by the CUDA-core path). */
-size_t moda_fwd_workspace_bytes(const moda_desc* desc);
-
 /* Forward (the operation above).
  * In:  q, k, v, kd, vd (device, desc->dtype; kd/vd may be NULL when S == 0).
  * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it).
- * Workspace: device scratch of at least moda_fwd_workspace_bytes(desc) bytes,
- * 256-byte aligned, owned by the caller and not used concurrently by another call;
- * its contents on entry do not matter.  May be NULL when that size is 0
- * (MODA_ERR_WORKSPACE otherwise).
- * bf16 with d in {64, 128}, G = H/Hkv <= 8 and S <= 64 runs on the tensor cores
- * (tcgen05, float32 accumulation, P rounded to bf16 for the PV products of both
- * memories); other bf16 shapes and float32 run on the CUDA cores in float32. */
+ * bf16 with d in {64, 128} runs on the tensor cores: tcgen05 MMAs with float32
+ * accumulation for both memories (the depth slots of each query's position enter as
+ * extra, block-masked key tiles of the same online softmax), P rounded to bf16 for the
+ * PV products; float32 runs on the CUDA cores in float32. */
 moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
-                     const void* vd, void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+                     const void* vd, void* o, float* lse, void* stream);
 
 /* Bytes of device workspace moda_bwd needs for `desc` (float32 row statistics
  * and the float32 dq accumulator).  0 on invalid desc. */

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MODA_OK", 1: "MODA_ERR_INVALID_ARG", 2: "MODA_ERR_UNSUPPORTE
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 # Names of every function include/moda.h declares.
-EXPORTS = ("moda_fwd", "moda_fwd_workspace_bytes", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status",
+EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status",
            "moda_status_str",
            "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
            "moda_bwd_profiled", "moda_selftest_wait_timeout")
@@ -54,10 +54,8 @@ def load_library():
                 raise RuntimeError(f"libmoda.so is not built ({_build.LIB}); run __graft_entry__.build()")
             lib = ctypes.CDLL(_build.LIB)
             p, d = ctypes.c_void_p, ctypes.POINTER(moda_desc)
-            lib.moda_fwd.argtypes = [d, p, p, p, p, p, p, p, p, ctypes.c_size_t, p]
+            lib.moda_fwd.argtypes = [d, p, p, p, p, p, p, p, p]
             lib.moda_fwd.restype = ctypes.c_int
-            lib.moda_fwd_workspace_bytes.argtypes = [d]
-            lib.moda_fwd_workspace_bytes.restype = ctypes.c_size_t
             lib.moda_bwd_workspace_bytes.argtypes = [d]
             lib.moda_bwd_workspace_bytes.restype = ctypes.c_size_t
             lib.moda_bwd.argtypes = [d] + [p] * 14 + [ctypes.c_size_t, p]
@@ -114,15 +112,8 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def moda_fwd_workspace_bytes(desc: moda_desc) -> int:
-    """Workspace bytes moda_fwd needs on the current device (0: none)."""
-    return int(load_library().moda_fwd_workspace_bytes(ctypes.byref(desc)))
-
-
-def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None, workspace=None):
-    """Joint sequence/depth attention forward.  Returns (o [B,H,T,d], lse [B,H,T] float32).
-    ``workspace`` (uint8 CUDA tensor of at least moda_fwd_workspace_bytes) is allocated
-    here when not given."""
+def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None):
+    """Joint sequence/depth attention forward.  Returns (o [B,H,T,d], lse [B,H,T] float32)."""
     desc = _desc_from(q, k, kd, scale)
     B, H, T, d = q.shape
     for t, name in ((k, "k"), (v, "v")):
@@ -134,14 +125,8 @@ def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None, workspa
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    need = moda_fwd_workspace_bytes(desc)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_ptr = _ptr(workspace) if workspace is not None else None
-    ws_bytes = workspace.numel() if workspace is not None else 0
     st = load_library().moda_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None,
-                                 _ptr(vd) if desc.S else None, _ptr(o), _ptr(lse), ws_ptr, ctypes.c_size_t(ws_bytes),
-                                 _stream(stream))
+                                 _ptr(vd) if desc.S else None, _ptr(o), _ptr(lse), _stream(stream))
     if st != MODA_OK:
         raise MODAError(st, "moda_fwd")
     return o, lse

@@ -102,24 +102,14 @@ size_t dq_accum_bytes(const moda_desc* d) {
 
 extern "C" {
 
-size_t moda_fwd_workspace_bytes(const moda_desc* desc) {
-  if (check_desc(desc) != MODA_OK) return 0;
-  if (desc->dtype != MODA_DTYPE_BF16) return 0;
-  const moda::Problem p = problem_of(desc);
-  return moda::fwd_sm103_supported(p) ? align256(moda::fwd_sm103_workspace_bytes(p)) : 0;
-}
-
 moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
-                     const void* vd, void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                     const void* vd, void* o, float* lse, void* stream) {
   moda_status st = check_desc(desc);
   if (st != MODA_OK) return st;
   if (!q || !k || !v || !o) return MODA_ERR_INVALID_ARG;
   if (desc->S > 0 && (!kd || !vd)) return MODA_ERR_INVALID_ARG;
   for (const void* p : {q, k, v, kd, vd, static_cast<const void*>(o), static_cast<const void*>(lse)})
     if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
-  const size_t need = moda_fwd_workspace_bytes(desc);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MODA_ERR_WORKSPACE;
-  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MODA_ERR_INVALID_ARG;
   moda::FwdArgs a;
   a.p = problem_of(desc);
   a.status = status_word();
@@ -131,8 +121,6 @@ moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const 
   a.vd = desc->S > 0 ? vd : nullptr;
   a.o = o;
   a.lse = lse;
-  a.scratch = workspace;
-  a.scratch_bytes = workspace_bytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (desc->dtype == MODA_DTYPE_BF16 && moda::fwd_sm103_supported(a.p))

@@ -28,9 +28,7 @@ struct FwdArgs {
   int* status;  // device status word (bounded-wait timeouts)
   const void *q, *k, *v, *kd, *vd;
   void* o;
-  float* lse;            // may be null
-  void* scratch;         // workspace of the tensor-core path (depth partial states), may be null
-  size_t scratch_bytes;
+  float* lse;  // may be null
 };
 
 struct BwdArgs {
@@ -75,7 +73,6 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s)
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s);
 bool fwd_sm103_supported(const Problem& p);
-size_t fwd_sm103_workspace_bytes(const Problem& p);  // 0 when none is needed
 bool bwd_sm103_supported(const Problem& p);
 
 }  // namespace moda

@@ -59,7 +59,7 @@ FAKE = 1 << 20  # aligned fake device address: validation must fail before any u
 
 def fwd(lib, d, ptrs=None):
     p = [ctypes.c_void_p(FAKE)] * 7 if ptrs is None else ptrs
-    return lib.moda_fwd(ctypes.byref(d) if d is not None else None, *p, None, 0, None)
+    return lib.moda_fwd(ctypes.byref(d) if d is not None else None, *p, None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -99,10 +99,3 @@ def test_backward_workspace_contract(lib):
     assert lib.moda_bwd(ctypes.byref(d), *ptrs, None, ctypes.c_size_t(need), None) == 5
     # workspace not 256-byte aligned
     assert lib.moda_bwd(ctypes.byref(d), *ptrs, ctypes.c_void_p(FAKE + 16), ctypes.c_size_t(need), None) == 1
-
-
-def test_forward_workspace_size_for_invalid_and_cuda_core_shapes(lib):
-    assert lib.moda_fwd_workspace_bytes(None) == 0
-    assert lib.moda_fwd_workspace_bytes(ctypes.byref(desc(H=3, Hkv=2))) == 0
-    assert lib.moda_fwd_workspace_bytes(ctypes.byref(desc(dtype=0))) == 0  # float32: CUDA-core path
-    assert lib.moda_fwd_workspace_bytes(ctypes.byref(desc(S=0))) == 0  # no depth state to keep

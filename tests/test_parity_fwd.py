@@ -96,23 +96,3 @@ def test_forward_is_deterministic_and_sync_status_clean(monkeypatch):
     o2, l2 = run_fwd(x)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert binding.moda_device_status() == 0
-
-
-def test_forward_workspace_too_small_is_refused():
-    """The tensor-core forward keeps per-CTA depth states in the caller's workspace: a
-    workspace below moda_fwd_workspace_bytes is refused before anything is launched."""
-    shape = Shape("ws", 1, 8, 2, 300, 128, 6, bf16)
-    x = make_inputs(shape, seed=5)
-    g = {k: v.cuda() for k, v in x.items()}
-    desc = binding.make_desc(1, 8, 2, 300, 6, 128, bf16)
-    need = binding.moda_fwd_workspace_bytes(desc)
-    assert need > 0
-    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
-    with pytest.raises(binding.MODAError) as err:
-        binding.moda_fwd(g["q"], g["k"], g["v"], g["kd"], g["vd"], workspace=small)
-    assert err.value.status == 5  # MODA_ERR_WORKSPACE
-    o, lse = binding.moda_fwd(g["q"], g["k"], g["v"], g["kd"], g["vd"],
-                              workspace=torch.empty(need, dtype=torch.uint8, device="cuda"))
-    torch.cuda.synchronize()
-    ro, _ = oracle.forward(*(host_view(x[n]) for n in ("q", "k", "v", "kd", "vd")))
-    assert max_abs(as_f64(o), ro) < TOL_OUT[bf16]
