@@ -74,11 +74,19 @@ struct FwdCfg {
   static constexpr int OFF_KV = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE_BYTES;
   // kv_full[NSLOT], kv_empty[NSLOT], q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2],
-  // o_free[2], drain
-  static constexpr int NBAR = 2 * NSLOT + 13;
+  // o_free[2], s_free[2], drain[2]
+  static constexpr int NBAR = 2 * NSLOT + 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr uint32_t TM_O = 256;  // O_t at TM_O + t*D; S_t at t*BN
   static_assert(SMEM <= kSmemLimit, "shared memory");
+  // TMEM columns.  SPLIT (d = 64): S_t, P_t, O_t of tile t each in columns of their own,
+  // [256t, +128), [256t + 128, +64), [256t + 192, +64), so S of the next key tile can be
+  // computed while the softmax of this one still runs.  Otherwise (d = 128) there is room
+  // for S and O only: P_t is packed into the first 64 columns of S_t, S_t at 128t, O_t at
+  // 256 + 128t, and the next S waits until the PV that reads P was issued.
+  static constexpr bool SPLIT = D == 64;
+  static constexpr uint32_t tm_s(int t) { return SPLIT ? 256u * t : 128u * t; }
+  static constexpr uint32_t tm_p(int t) { return SPLIT ? 256u * t + 128u : 128u * t; }
+  static constexpr uint32_t tm_o(int t) { return SPLIT ? 256u * t + 192u : 256u + D * t; }
 };
 
 struct FwdTcParams {
@@ -168,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_free = pv_done + 2;
-  uint64_t* drain = o_free + 2;
+  uint64_t* s_free = o_free + 2;
+  uint64_t* drain = s_free + 2;
   uint8_t* misc = smem + C::OFF_BAR + C::NBAR * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], C::SPLIT ? 2 : 1);  // released by each MMA issuer
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&q_full[t], 1);
@@ -185,8 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
       mbar_init(&o_free[t], 128);
+      mbar_init(&s_free[t], 4);  // one arrival per softmax warp (SPLIT)
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -268,8 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_issued1 > 0) mbar_wait(&q_full[1], (q_issued1 - 1) & 1, &never);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (!C::SPLIT && warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (d = 128)
+    // One thread for both tiles: PV_0(i), S_0(i+1), PV_1(i), S_1(i+1) in this order, since
+    // S of the next key tile overwrites P of this one.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int t, int item) {
         const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
         const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
-        const uint32_t d_tmem = tmem + t * BN;
+        const uint32_t d_tmem = tmem + C::tm_s(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ss(d_tmem, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
@@ -296,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int item, bool acc) {
         const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
-        const uint32_t p_tmem = tmem + t * BN;
+        const uint32_t p_tmem = tmem + C::tm_p(t);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_O + t * D, p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
+          mma_bf16_ts(tmem + C::tm_o(t), p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
                       (acc || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done[t]);
       };
@@ -433,9 +446,138 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         raise_abort(abort_flag, p.status);
         // wait for every MMA already issued before TMEM is released
-        mma_commit(drain);
+        mma_commit(&drain[0]);
         volatile int never = 0;
-        mbar_wait(drain, 0, &never);
+        mbar_wait(&drain[0], 0, &never);
+      }
+    }
+  } else if (C::SPLIT && (warp == 1 || warp == 2)) {
+    // ---------------------------------------------------------------- MMA issuers (d = 64)
+    // One thread per query tile t (warps 1 and 2), so neither tile's S/PV chain waits on
+    // the other's softmax.  Every K/V item is released twice: once by each tile that uses
+    // it, twice by its only user otherwise.
+    if (lane == 0) {
+      const int t = warp - 1;
+      constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
+      constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
+      static_assert((C::NSLOT & (C::NSLOT - 1)) == 0, "ring size");
+      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + t * C::TILE_BYTES, 16, 1024);
+      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);        // K-major (K tiles)
+      const uint64_t kv_desc_v = sdesc_sw128(sbase + C::OFF_KV, BN * 128, 1024);  // MN-major (V tiles)
+      const uint32_t s_tm = tmem + C::tm_s(t), p_tm = tmem + C::tm_p(t), o_tm = tmem + C::tm_o(t);
+      int base = 0;                     // first item of the unit
+      uint32_t scnt = 0, pcnt = 0;      // S issued, p_full phases consumed
+      bool ok = true;
+      auto wait_item = [&](int item) -> bool {
+        return mbar_wait(&kv_full[item % C::NSLOT], (item / C::NSLOT) & 1, abort_flag);
+      };
+      auto release = [&](int item, bool shared) {
+        mma_commit(&kv_empty[item % C::NSLOT]);
+        if (!shared) mma_commit(&kv_empty[item % C::NSLOT]);
+      };
+      auto issue_s = [&](int item) {
+        const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(s_tm, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                      sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
+        mma_commit(&s_full[t]);
+        ++scnt;
+      };
+      auto issue_pv = [&](int item, bool acc) {
+        const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(o_tm, p_tm + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done[t]);
+      };
+      for (int k = 0; ok && k < n_c; ++k) {
+        const Unit u = unit_at(p, cta, k);
+        const bool two = u.ns[1] > 0;
+        const int n_t = t ? u.ns[1] : u.ns[0];
+        const int nt_other = t ? u.nt[0] : u.nt[1];  // sequence tiles of the other query tile
+        const int sbase = base + u.nd_items, st = two ? 4 : 2;
+        // K and V items of step i of this tile, and whether the other tile reads them too
+        auto kv = [&](int i, int& ki, int& vi) -> bool {
+          if (i < p.n_d) {
+            ki = base + st * i + t;
+            vi = base + st * i + (two ? 2 : 1) + t;
+            return false;
+          }
+          ki = sbase + 2 * (i - p.n_d);
+          vi = ki + 1;
+          return i - p.n_d < nt_other;
+        };
+        ok = mbar_wait(&q_full[t], k & 1, abort_flag);
+        if (!ok) break;
+        if (n_t == 0) {
+          mma_commit(&q_empty[t]);  // tile unused in this unit
+        } else {
+          // S of step 0
+          int ki, vi;
+          bool sh = kv(0, ki, vi);
+          if constexpr (C::SPLIT) {
+            if (scnt > 0 && !mbar_wait(&s_free[t], (scnt - 1) & 1, abort_flag)) ok = false;
+          }
+          if (ok && !wait_item(ki)) ok = false;
+          if (ok) {
+            tc_fence_after();
+            issue_s(ki);
+            if (n_t == 1) mma_commit(&q_empty[t]);
+            release(ki, sh);
+          }
+          for (int i = 0; ok && i < n_t; ++i) {
+            const bool more = i + 1 < n_t;
+            int kn = 0, vn = 0;
+            const bool sh_n = more ? kv(i + 1, kn, vn) : false;
+            sh = kv(i, ki, vi);
+            if constexpr (C::SPLIT) {
+              // S of step i+1 as soon as the softmax has read S of step i
+              if (more) {
+                if (!mbar_wait(&s_free[t], (scnt - 1) & 1, abort_flag) || !wait_item(kn)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_s(kn);
+                if (i + 2 == n_t) mma_commit(&q_empty[t]);
+                release(kn, sh_n);
+              }
+            }
+            // PV of step i once P is written
+            if (!wait_item(vi) || !mbar_wait(&p_full[t], pcnt & 1, abort_flag) ||
+                (i == 0 && k > 0 && !mbar_wait(&o_free[t], (k - 1) & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            ++pcnt;
+            tc_fence_after();
+            issue_pv(vi, i > 0);
+            release(vi, sh);
+            if constexpr (!C::SPLIT) {
+              // S of step i+1 overwrites P of step i: in-order execution of this thread's
+              // MMAs makes that safe once the PV reading it is issued
+              if (more) {
+                if (!wait_item(kn)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_s(kn);
+                if (i + 2 == n_t) mma_commit(&q_empty[t]);
+                release(kn, sh_n);
+              }
+            }
+          }
+        }
+        base = sbase + 2 * max(u.nt[0], u.nt[1]);
+      }
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        // wait for every MMA this thread issued before TMEM is released
+        mma_commit(&drain[t]);
+        volatile int never = 0;
+        mbar_wait(&drain[t], 0, &never);
       }
     }
   } else if (warp >= 4) {
@@ -444,8 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const int r = (wq << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_base + t * BN;
-    const uint32_t o_tmem = tmem + lane_base + C::TM_O + t * D;
+    const uint32_t s_tmem = tmem + lane_base + C::tm_s(t);
+    const uint32_t p_tmem = tmem + lane_base + C::tm_p(t);
+    const uint32_t o_tmem = tmem + lane_base + C::tm_o(t);
     const int pl = r / p.G, hl = r - pl * p.G;  // local position and head of row r
     // positions this warp's rows cover (for skipping depth tiles that miss them all)
     const int wp_lo = (wq * 32) / p.G, wp_hi = min(wq * 32 + 31, p.P * p.G - 1) / p.G;
@@ -470,11 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k0 = j * BN;
           if (wp_hi * p.S + p.S <= k0 || wp_lo * p.S >= k0 + BN) {
             // no position of this warp has keys in this depth tile: P = 0
+            if constexpr (C::SPLIT) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&s_free[t]);
+              if (j > 0) {  // P_t is still read by the previous PV until it completes
+                ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+              }
+            }
             uint32_t z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0u;
-            tmem_st32(s_tmem, z);
-            tmem_st32(s_tmem + 32, z);
+            tmem_st32(p_tmem, z);
+            tmem_st32(p_tmem + 32, z);
             tc_fence_before();
             mbar_arrive(&p_full[t]);
             ++jcnt;
@@ -487,11 +640,84 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo = 0;
           hi = (kb + BN - 1 > pfirst || !valid) ? (valid ? pos - kb + 1 : 0) : BN;
         }
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+        if constexpr (C::SPLIT) {
+          // S read whole, then handed back to the MMA issuer for the next key tile
+          uint32_t s[BN];
+          tmem_ld128(s_tmem, s);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[t]);
+          if (lo > 0 || hi < BN) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (c < lo || c >= hi) s[c] = __float_as_uint(-INFINITY);
+          }
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < BN; c += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+          }
+          const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+          bool pv_waited = j == 0;  // P_t is free once the previous PV of this tile completed
+          const bool need = m_tile > m_run + kRescaleThreshold;  // includes the first keys of a row
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? fmaxf(m_run, m_tile) : m_run;
+            // a row that holds no mass yet (m_run = -inf) needs no rescale of O or l
+            const float corr = (m_run == -INFINITY || !need) ? 1.f : ex2(m_run - m_new);
+            if (__any_sync(0xffffffffu, corr != 1.f)) {
+              // the previous PV of this tile must have landed in O before it is rescaled
+              ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              pv_waited = true;
+#pragma unroll 1
+              for (int c = 0; c < D / 16; ++c) {
+                uint32_t o[16];
+                tmem_ld16(o_tmem + c * 16, o);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                tmem_st16(o_tmem + c * 16, o);
+              }
+            }
+            l_run *= corr;
+            m_run = m_new;
+          }
+          if (!pv_waited) {
+            ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = half * 64; c < half * 64 + 64; c += 4) {
+              float x0, x1, x2, x3;
+              ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
+              ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
+              x0 = ex2(x0);
+              x1 = ex2(x1);
+              x2 = ex2(x2);
+              x3 = ex2(x3);
+              if ((c & 4) == 0)
+                fadd2(ls0, ls1, x0, x1), fadd2(ls0, ls1, x2, x3);
+              else
+                fadd2(ls2, ls3, x0, x1), fadd2(ls2, ls3, x2, x3);
+              pk[(c - half * 64) >> 1] = pack_bf16(x0, x1);
+              pk[((c - half * 64) >> 1) + 1] = pack_bf16(x2, x3);
+            }
+            tmem_st32(p_tmem + half * 32, pk);
+          }
+        } else {
         // Two halves of 64 keys.  P of the first half is written (over S columns already
         // read) before the second half is loaded; if the second half raises the running max
         // of a row that holds mass past the threshold, the first half's P is rescaled in
         // place together with O and l.
-        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t s[64];
@@ -565,6 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[(c >> 1) + 1] = pack_bf16(x2, x3);
           }
           tmem_st32(s_tmem + half * 32, pk);
+        }
         }
         if (!ok) break;
         l_run += (ls0 + ls1) + (ls2 + ls3);
