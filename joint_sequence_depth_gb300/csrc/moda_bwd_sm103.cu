@@ -801,6 +801,626 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   }
 }
 
+// ============================================================================ dK / dV, d = 64
+// CTA: 128 keys [kb, kb+128) of (b, g).  Query tiles of 128 rows, head-major inside the
+// tile (row r -> head g*G + r/P2, position p0 + r%P2, P2 = floor(128/G)), so the S^T and
+// dP^T products have N = 128.  One CTA per SM, 320 threads.
+// TMEM (512 columns): S^T [0,128), dP^T [128,256), P^T [256,320) and dS^T [320,384)
+// (bf16 pairs), dV [384,448), dK [448,512).  The gradient warps release S^T/dP^T as soon
+// as they have read them (s_free), so S^T and dP^T of tile i+1 are computed while P^T and
+// dS^T of tile i are formed; dV, dK of tile i follow (p_full) and free P^T, dS^T (p_free).
+// Warps: 0 loads, 1 MMA issuer, 2..9 gradient warps: warpgroup w forms query columns
+// [64w, 64w+64) of every tile; thread = key = TMEM lane.
+constexpr int K2N = 128;
+
+struct Dkv64Cfg {
+  static constexpr int D = 64;
+  static constexpr int THREADS = 64 + 256;
+  static constexpr int KV_BYTES = KBM * D * 2;    // the CTA's K (or V) tile
+  static constexpr int QT_BYTES = K2N * D * 2;    // one 128-row Q (or dO) tile
+  static constexpr int NSTAGE = 4;
+  static constexpr int STAGE_BYTES = 2 * QT_BYTES;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_BYTES;
+  static constexpr int OFF_Q = 2 * KV_BYTES;      // stage s: Q at + s*STAGE, dO at + QT_BYTES
+  static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][128] {-lse*log2e, Delta}
+  static constexpr int OFF_BAR = OFF_STAT + NSTAGE * K2N * 8;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, p_free, drain, last_done
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 6;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_P = 256, TM_DS = 320, TM_DV = 384, TM_DK = 448;
+  static constexpr uint32_t TM_COLS = 512;
+};
+
+__global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
+    moda_bwd_dkdv64_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                           const BwdTcParams p) {
+  using C = Dkv64Cfg;
+  constexpr int D = C::D;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kStatusConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P2 = K2N / p.G;  // positions per query tile
+  const int ngroups = p.B * p.Hkv;
+  const int kblk = static_cast<int>(blockIdx.x) / ngroups;  // smallest key blocks (most query tiles) first
+  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int kb = kblk * KBM;
+  const int qt0 = kb / P2, qt1 = (p.T - 1) / P2;
+  const int n_q = qt1 - qt0 + 1;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::NSTAGE;
+  uint64_t* s_full = q_empty + C::NSTAGE;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* p_full = s_free + 1;
+  uint64_t* p_free = p_full + 1;
+  uint64_t* drain = p_free + 1;
+  uint64_t* last_done = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  // per stage: -lse*log2(e) of the 128 rows, then Delta of the 128 rows (four rows per float4)
+  const float4* stat = reinterpret_cast<const float4*>(smem + C::OFF_STAT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(&q_full[i], 1 + 32);  // TMA arrive + one cp.async arrival per producer lane
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 8);  // one arrival per gradient warp
+    mbar_init(p_full, 8);
+    mbar_init(p_free, 1);
+    mbar_init(drain, 1);
+    mbar_init(last_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // rows past P2*G of every query tile are never written by TMA: zero them once
+  if (P2 * p.G < K2N) {
+    for (int i = threadIdx.x; i < C::NSTAGE * C::STAGE_BYTES / 16; i += blockDim.x)
+      st_shared_v4(sbase + C::OFF_Q + i * 16, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- loads
+    bool ok = true;
+    int issued = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      tma_load_3d(smem + C::OFF_K, &tmK, kv_full, 0, kb, bg);
+      tma_load_3d(smem + C::OFF_V, &tmV, kv_full, 0, kb, bg);
+    }
+    for (int i = 0; i < n_q; ++i) {
+      const int st = i % C::NSTAGE, use = i / C::NSTAGE;
+      if (use > 0 && !warp_wait(&q_empty[st], (use - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int p0 = (qt0 + i) * P2;
+      // row statistics (LSE, Delta) of this tile, copied asynchronously.  Rows that do not
+      // exist (head >= G or position >= T) read a valid row's statistics: their Q and dO rows
+      // are zero in shared memory, so whatever finite P and dS they get contributes nothing.
+      const uint32_t sl = sbase + C::OFF_STAT + st * K2N * 8;
+#pragma unroll
+      for (int rr = 0; rr < K2N / 32; ++rr) {
+        const int r = lane + 32 * rr;
+        const int hh = min(r / P2, p.G - 1), pos = min(p0 + r % P2, p.T - 1);
+        const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + pos;
+        const float* src = reinterpret_cast<const float*>(p.stats + row);
+        cp_async_4(sl + r * 4, src);
+        cp_async_4(sl + K2N * 4 + r * 4, src + 1);
+      }
+      cp_async_arrive_noinc(&q_full[st]);
+      if (lane == 0) {
+        uint8_t* dst = smem + C::OFF_Q + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&q_full[st], static_cast<uint32_t>(2 * P2 * p.G * D * 2));
+        tma_load_3d(dst, &tmQ, &q_full[st], 0, p0, b * p.H + g * p.G);
+        tma_load_3d(dst + C::QT_BYTES, &tmO, &q_full[st], 0, p0, b * p.H + g * p.G);
+      }
+      issued = i + 1;
+    }
+    if (!ok || *abort_flag) {
+      if (lane == 0) {
+        raise_abort(abort_flag, p.status);
+        volatile int never = 0;
+        mbar_wait(kv_full, 0, &never);
+      }
+      volatile int never = 0;
+      for (int i = max(0, issued - C::NSTAGE); i < issued; ++i)
+        mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(KBM, K2N, false);
+      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
+      const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t qt_desc_k = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);          // K-major Q/dO tiles
+      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, K2N * 128, 1024);  // MN-major Q/dO tiles
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      for (int i = 0; ok && i <= n_q; ++i) {
+        if (i < n_q) {
+          // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, once tile i is loaded and the gradient
+          // warps have read S^T/dP^T of tile i-1
+          const int st = i % C::NSTAGE;
+          ok = mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag) &&
+               (i == 0 || mbar_wait(s_free, (i - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t q_desc = sdesc_add(qt_desc_k, st * C::STAGE_BYTES);
+          const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + C::TM_S, sdesc_add(k_desc, kk * 32), sdesc_add(q_desc, kk * 32), IDESC_S, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + C::TM_DP, sdesc_add(v_desc, kk * 32), sdesc_add(o_desc, kk * 32), IDESC_S, kk > 0);
+          mma_commit(s_full);
+        }
+        if (i > 0) {
+          // dV += P^T(j) dO_j, dK += dS^T(j) Q_j for j = i-1
+          const int j = i - 1, st = j % C::NSTAGE;
+          ok = mbar_wait(p_full, j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
+          const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < K2N / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < K2N / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DS + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&q_empty[st]);
+          mma_commit(p_free);
+        }
+      }
+      if (ok) mma_commit(last_done);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- gradients (thread = key)
+    const int wg = (warp - 2) >> 2;
+    const int kr = ((warp & 3) << 5) + lane;
+    const int key = kb + kr;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool pow2 = (P2 & (P2 - 1)) == 0;
+    bool ok = true;
+    for (int i = 0; i < n_q; ++i) {
+      ok = warp_wait(s_full, i & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[64], dpv[64];
+      tmem_ld64x2(tmem + lane_base + C::TM_S + wg * 64, tmem + lane_base + C::TM_DP + wg * 64, s, dpv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      const int st = i % C::NSTAGE;
+      const float4* sl = stat + st * (K2N / 2);  // [0, 32): -lse2 of rows 4c..4c+3; [32, 64): Delta
+      const int p0 = (qt0 + i) * P2;
+      const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
+      const int dk = key - p0;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = wg * 64 + hf * 32;  // first query column of this group
+        float e[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 ls = sl[(c0 + c) >> 2];  // -lse2 of rows c0+c .. c0+c+3
+          ffma2(__uint_as_float(s[hf * 32 + c]), __uint_as_float(s[hf * 32 + c + 1]), sl2, sl2, ls.x, ls.y, e[c],
+                e[c + 1]);
+          ffma2(__uint_as_float(s[hf * 32 + c + 2]), __uint_as_float(s[hf * 32 + c + 3]), sl2, sl2, ls.z, ls.w,
+                e[c + 2], e[c + 3]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) e[c + u] = ex2(e[c + u]);
+        }
+        if (diag) {
+          // row r sits at position p0 + r % P2 (head-major tile); keys after it are masked
+          if (pow2) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) e[c] = (dk > ((c0 + c) & (P2 - 1))) ? 0.f : e[c];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) e[c] = (dk > (c0 + c) % P2) ? 0.f : e[c];
+          }
+        }
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 dl = sl[K2N / 4 + ((c0 + c) >> 2)];  // Delta of rows c0+c .. c0+c+3
+          float d0, d1, d2, d3;
+          fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dl.x, dl.y, e[c],
+                   e[c + 1], d0, d1);
+          fsubmul2(__uint_as_float(dpv[hf * 32 + c + 2]), __uint_as_float(dpv[hf * 32 + c + 3]), dl.z, dl.w,
+                   e[c + 2], e[c + 3], d2, d3);
+          pp[c >> 1] = pack_bf16(e[c], e[c + 1]);
+          pp[(c >> 1) + 1] = pack_bf16(e[c + 2], e[c + 3]);
+          pd[c >> 1] = pack_bf16(d0, d1);
+          pd[(c >> 1) + 1] = pack_bf16(d2, d3);
+        }
+        // P^T and dS^T of tile i-1 must have been read by its dV/dK products first
+        if (hf == 0 && i > 0) {
+          ok = warp_wait(p_free, (i - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st16_nowait(tmem + lane_base + C::TM_P + wg * 32 + hf * 16, pp);
+        tmem_st16_nowait(tmem + lane_base + C::TM_DS + wg * 32 + hf * 16, pd);
+      }
+      if (!ok) break;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (!ok) {
+      raise_abort(abort_flag, p.status);
+    } else {
+      ok = warp_wait(last_done, 0, abort_flag);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+      } else {
+        tc_fence_after();
+        // dV (warpgroup 0) and dK (scaled; warpgroup 1)
+        const uint32_t src = wg == 0 ? C::TM_DV : C::TM_DK;
+        __nv_bfloat16* out = (wg == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
+        const float mul = wg == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t acc[32];
+          tmem_ld32(tmem + lane_base + src + c0, acc);
+          if (key < p.T) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(
+                  pack_bf16(__uint_as_float(acc[8 * u]) * mul, __uint_as_float(acc[8 * u + 1]) * mul),
+                  pack_bf16(__uint_as_float(acc[8 * u + 2]) * mul, __uint_as_float(acc[8 * u + 3]) * mul),
+                  pack_bf16(__uint_as_float(acc[8 * u + 4]) * mul, __uint_as_float(acc[8 * u + 5]) * mul),
+                  pack_bf16(__uint_as_float(acc[8 * u + 6]) * mul, __uint_as_float(acc[8 * u + 7]) * mul));
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+// ============================================================================ dQ, d = 64
+// CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G, head
+// g*G + r%G), P = floor(128/G) positions.  Key tiles of 128, so S and dP have N = 128.
+// One CTA per SM, 320 threads.  TMEM (512 columns): S [0,128), dP [128,256) (released as
+// soon as the gradient warps have read them, so S and dP of tile j+1 are computed while
+// dS of tile j is formed), dS[2] [256,320), [320,384) (bf16 pairs, double-buffered),
+// dQ [384,448).  Warps: 0 loads K_j, V_j; 1 MMA issuer; 2..9 gradient warps (warpgroup w
+// forms key columns [64w, 64w+64) of every tile; warpgroup 0 also stages Q and dO).
+constexpr int Q2N = 128;
+
+struct Dq64Cfg {
+  static constexpr int D = 64;
+  static constexpr int THREADS = 64 + 256;
+  static constexpr int KV_BYTES = Q2N * D * 2;  // one K (or V) tile; a ring slot holds both
+  static constexpr int NSLOT = 3;
+  static constexpr int Q_BYTES = QBM * D * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = Q_BYTES;
+  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, ds_free[2], drain, last_done
+  static constexpr int NBAR = 2 * NSLOT + 8;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DS = 256, TM_DQ = 384;
+  static constexpr uint32_t TM_COLS = 512;
+};
+
+__global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
+    moda_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const BwdTcParams p) {
+  using C = Dq64Cfg;
+  constexpr int D = C::D;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kStatusConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = QBM / p.G;
+  const int n_pb = (p.T + P - 1) / P;
+  const int ngroups = p.B * p.Hkv;
+  const int pb = n_pb - 1 - static_cast<int>(blockIdx.x) / ngroups;  // longest rows first
+  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int p0 = pb * P;
+  const int p_last = min(p0 + P, p.T) - 1;
+  const int n_kv = p_last / Q2N + 1;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + C::NSLOT;
+  uint64_t* q_full = bars + 2 * C::NSLOT;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* ds_full = s_free + 1;
+  uint64_t* ds_free = ds_full + 1;  // [2]
+  uint64_t* drain = ds_free + 2;
+  uint64_t* last_done = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(q_full, 128);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 8);  // one arrival per gradient warp
+    mbar_init(ds_full, 8);
+    mbar_init(&ds_free[0], 1);
+    mbar_init(&ds_free[1], 1);
+    mbar_init(drain, 1);
+    mbar_init(last_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- K_j, V_j loads
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j % C::NSLOT, use = j / C::NSLOT;
+        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
+          raise_abort(abort_flag, p.status);
+          break;
+        }
+        uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
+        mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+        tma_load_3d(dst, &tmK, &kv_full[slot], 0, j * Q2N, bg);
+        tma_load_3d(dst + C::KV_BYTES, &tmV, &kv_full[slot], 0, j * Q2N, bg);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        for (int j = max(0, issued - C::NSLOT); j < issued; ++j)
+          mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(QBM, Q2N, false);
+      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
+      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t do_desc = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);           // K-major
+      const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, Q2N * 128, 1024);   // MN-major
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        if (j < n_kv) {
+          // S(j) = Q K_j^T and dP(j) = dO V_j^T, once K_j, V_j are loaded and the gradient
+          // warps have read S/dP of tile j-1
+          const int slot = j % C::NSLOT;
+          ok = mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag) &&
+               (j == 0 || mbar_wait(s_free, (j - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
+          const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + C::TM_S, sdesc_add(q_desc, kk * 32), sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + C::TM_DP, sdesc_add(do_desc, kk * 32), sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
+          mma_commit(s_full);
+        }
+        if (j > 0) {
+          // dQ += dS(jj) K_jj for jj = j-1
+          const int jj = j - 1, slot = jj % C::NSLOT;
+          ok = mbar_wait(ds_full, jj & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
+          const uint32_t ds = C::TM_DS + (jj & 1) * 64;
+#pragma unroll
+          for (int kk = 0; kk < Q2N / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&kv_empty[slot]);  // K_jj, V_jj no longer read
+          mma_commit(&ds_free[jj & 1]);
+        }
+      }
+      if (ok) mma_commit(last_done);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- gradients (thread = row)
+    const int wg = (warp - 2) >> 2;
+    const int r = ((warp & 3) << 5) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int pos = p0 + r / p.G;
+    const bool valid = (r < P * p.G) && pos < p.T;
+    const int h = g * p.G + r % p.G;
+    const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
+    if (wg == 0) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
+      const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {
+        const uint32_t off = sw128_offset(r, ch);
+        st_shared_v4(sbase + C::OFF_Q + off, valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0));
+        st_shared_v4(sbase + C::OFF_DO + off, valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0));
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const float2 stt = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
+    const float nlse2 = stt.x;  // -lse * log2(e)
+    const float dlt = stt.y;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = warp_wait(s_full, j & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[64], dpv[64];
+      tmem_ld64x2(tmem + lane_base + C::TM_S + wg * 64, tmem + lane_base + C::TM_DP + wg * 64, s, dpv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      const uint32_t ds = C::TM_DS + (j & 1) * 64 + wg * 32;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int lim = valid ? pos - (j * Q2N + wg * 64 + hf * 32) : -1;  // columns c <= lim are visible
+        float e[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          ffma2(__uint_as_float(s[hf * 32 + c]), __uint_as_float(s[hf * 32 + c + 1]), sl2, sl2, nlse2, nlse2, e[c],
+                e[c + 1]);
+          e[c] = ex2(e[c]);
+          e[c + 1] = ex2(e[c + 1]);
+        }
+        if (lim < 31) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float d0, d1;
+          fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dlt, dlt, e[c],
+                   e[c + 1], d0, d1);
+          pk[c >> 1] = pack_bf16(d0, d1);
+        }
+        // dS buffer (j & 1) was last read by the dQ product of tile j-2
+        if (hf == 0 && j >= 2) {
+          ok = warp_wait(&ds_free[j & 1], ((j >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st16_nowait(tmem + lane_base + ds + hf * 16, pk);
+      }
+      if (!ok) break;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (!ok) {
+      raise_abort(abort_flag, p.status);
+    } else {
+      ok = warp_wait(last_done, 0, abort_flag);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+      } else {
+        tc_fence_after();
+        // warpgroup w writes dq columns [32w, 32w+32)
+        const int c0 = wg * 32;
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
+        float extra[32];
+        if (p.S > 0 && valid) {
+          const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 e4 = src[i];
+            extra[4 * i] = e4.x;
+            extra[4 * i + 1] = e4.y;
+            extra[4 * i + 2] = e4.z;
+            extra[4 * i + 3] = e4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int c = 8 * i + 2 * k2;
+              w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
+                                fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
+            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
 // ============================================================================ host
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -889,26 +1509,43 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
       !make_map(&tk64, a.k, D, pr.T, planes_kv, QBN, 1) || !make_map(&tv64, a.v, D, pr.T, planes_kv, QBN, 1) ||
       !make_map(&tq, a.q, D, pr.T, planes_q, pq, pr.G) || !make_map(&to, a.dout, D, pr.T, planes_q, pq, pr.G))
     return cudaErrorInvalidValue;
-  // d = 64: single-buffered TMEM (256 columns), 192 threads, two CTAs per SM.
-  // d = 128: double-buffered TMEM, two gradient warpgroups, one CTA per SM.
-  constexpr int KNB = D == 64 ? 1 : 2, KNW = KNB;
-  constexpr int QNB = D == 64 ? 1 : 2, QNW = QNB;
-  using KC = DkvCfg<D, KNB, KNW>;
-  using QC = DqCfg<D, QNB, QNW>;
-  static int smem_dkdv = 0, smem_dq = 0;
-  e = set_smem(moda_bwd_dkdv_kernel<D, KNB, KNW>, KC::SMEM, smem_dkdv);
-  if (e != cudaSuccess) return e;
-  e = set_smem(moda_bwd_dq_kernel<D, QNB, QNW>, QC::SMEM, smem_dq);
-  if (e != cudaSuccess) return e;
   const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
-  mark_event(a, 4, s);
-  moda_bwd_dkdv_kernel<D, KNB, KNW><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
-  mark_event(a, 5, s);
   const int P = QBM / pr.G;
   const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
-  mark_event(a, 6, s);
-  moda_bwd_dq_kernel<D, QNB, QNW><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
-  mark_event(a, 7, s);
+  if constexpr (D == 64) {
+    // 128-column query / key tiles, S/dP released early, one CTA per SM (512 TMEM columns)
+    CUtensorMap tq2, to2;
+    const int pq2 = K2N / pr.G;
+    if (!make_map(&tq2, a.q, D, pr.T, planes_q, pq2, pr.G) || !make_map(&to2, a.dout, D, pr.T, planes_q, pq2, pr.G))
+      return cudaErrorInvalidValue;
+    static int smem_dkdv = 0, smem_dq = 0;
+    e = set_smem(moda_bwd_dkdv64_kernel, Dkv64Cfg::SMEM, smem_dkdv);
+    if (e != cudaSuccess) return e;
+    e = set_smem(moda_bwd_dq64_kernel, Dq64Cfg::SMEM, smem_dq);
+    if (e != cudaSuccess) return e;
+    mark_event(a, 4, s);
+    moda_bwd_dkdv64_kernel<<<grid_kv, Dkv64Cfg::THREADS, Dkv64Cfg::SMEM, s>>>(tk128, tv128, tq2, to2, p);
+    mark_event(a, 5, s);
+    mark_event(a, 6, s);
+    moda_bwd_dq64_kernel<<<grid_q, Dq64Cfg::THREADS, Dq64Cfg::SMEM, s>>>(tk128, tv128, p);
+    mark_event(a, 7, s);
+  } else {
+    // d = 128: 64-column tiles, double-buffered TMEM, two gradient warpgroups splitting
+    // each tile's columns, one CTA per SM.
+    using KC = DkvCfg<D, 2, 2>;
+    using QC = DqCfg<D, 2, 2>;
+    static int smem_dkdv = 0, smem_dq = 0;
+    e = set_smem(moda_bwd_dkdv_kernel<D, 2, 2>, KC::SMEM, smem_dkdv);
+    if (e != cudaSuccess) return e;
+    e = set_smem(moda_bwd_dq_kernel<D, 2, 2>, QC::SMEM, smem_dq);
+    if (e != cudaSuccess) return e;
+    mark_event(a, 4, s);
+    moda_bwd_dkdv_kernel<D, 2, 2><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
+    mark_event(a, 5, s);
+    mark_event(a, 6, s);
+    moda_bwd_dq_kernel<D, 2, 2><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
+    mark_event(a, 7, s);
+  }
   count_launches(2);
   return cudaGetLastError();
 }
@@ -923,3 +1560,4 @@ cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s) {
 }
 
 }  // namespace moda
+
