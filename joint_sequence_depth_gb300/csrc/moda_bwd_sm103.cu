@@ -808,7 +808,8 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), P^T [256,320) and dS^T [320,384)
 // (bf16 pairs), dV [384,448), dK [448,512).  The gradient warps release S^T/dP^T as soon
 // as they have read them (s_free), so S^T and dP^T of tile i+1 are computed while P^T and
-// dS^T of tile i are formed; dV, dK of tile i follow (p_full) and free P^T, dS^T (p_free).
+// dS^T of tile i are formed; dV, dK of tile i follow (p_full), and their commit (q_empty)
+// frees both the Q/dO stage and P^T, dS^T.
 // Warps: 0 loads, 1 MMA issuer, 2..9 gradient warps: warpgroup w forms query columns
 // [64w, 64w+64) of every tile; thread = key = TMEM lane.
 constexpr int K2N = 128;
@@ -825,7 +826,7 @@ struct Dkv64Cfg {
   static constexpr int OFF_Q = 2 * KV_BYTES;      // stage s: Q at + s*STAGE, dO at + QT_BYTES
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][128] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * K2N * 8;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, p_free, drain, last_done
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, (spare), drain, last_done
   static constexpr int NBAR = 1 + 2 * NSTAGE + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
@@ -862,8 +863,7 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
   uint64_t* s_full = q_empty + C::NSTAGE;
   uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;
-  uint64_t* p_free = p_full + 1;
-  uint64_t* drain = p_free + 1;
+  uint64_t* drain = p_full + 2;
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -879,7 +879,6 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);  // one arrival per gradient warp
     mbar_init(p_full, 8);
-    mbar_init(p_free, 1);
     mbar_init(drain, 1);
     mbar_init(last_done, 1);
     *abort_flag = 0;
@@ -999,8 +998,7 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
           for (int kk = 0; kk < K2N / 16; ++kk)
             mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DS + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
                         (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&q_empty[st]);
-          mma_commit(p_free);
+          mma_commit(&q_empty[st]);  // also tells the gradient warps that P^T(j), dS^T(j) are read
         }
       }
       if (ok) mma_commit(last_done);
@@ -1073,8 +1071,9 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
           pd[(c >> 1) + 1] = pack_bf16(d2, d3);
         }
         // P^T and dS^T of tile i-1 must have been read by its dV/dK products first
+        // (their commit completes tile i-1's phase of q_empty)
         if (hf == 0 && i > 0) {
-          ok = warp_wait(p_free, (i - 1) & 1, abort_flag);
+          ok = warp_wait(&q_empty[(i - 1) % C::NSTAGE], ((i - 1) / C::NSTAGE) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
         }
@@ -1147,7 +1146,7 @@ struct Dq64Cfg {
   static constexpr int OFF_DO = Q_BYTES;
   static constexpr int OFF_KV = 2 * Q_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, ds_free[2], drain, last_done
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, (2 spare), drain, last_done
   static constexpr int NBAR = 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
@@ -1184,8 +1183,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   uint64_t* s_full = q_full + 1;
   uint64_t* s_free = s_full + 1;
   uint64_t* ds_full = s_free + 1;
-  uint64_t* ds_free = ds_full + 1;  // [2]
-  uint64_t* drain = ds_free + 2;
+  uint64_t* drain = ds_full + 3;
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -1199,8 +1197,6 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);  // one arrival per gradient warp
     mbar_init(ds_full, 8);
-    mbar_init(&ds_free[0], 1);
-    mbar_init(&ds_free[1], 1);
     mbar_init(drain, 1);
     mbar_init(last_done, 1);
     *abort_flag = 0;
@@ -1282,8 +1278,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
           for (int kk = 0; kk < Q2N / 16; ++kk)
             mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
                         (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&kv_empty[slot]);  // K_jj, V_jj no longer read
-          mma_commit(&ds_free[jj & 1]);
+          mma_commit(&kv_empty[slot]);  // K_jj, V_jj and dS(jj) no longer read
         }
       }
       if (ok) mma_commit(last_done);
@@ -1353,9 +1348,10 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
                    e[c + 1], d0, d1);
           pk[c >> 1] = pack_bf16(d0, d1);
         }
-        // dS buffer (j & 1) was last read by the dQ product of tile j-2
+        // dS buffer (j & 1) was last read by the dQ product of tile j-2 (its commit
+        // completes tile j-2's phase of kv_empty)
         if (hf == 0 && j >= 2) {
-          ok = warp_wait(&ds_free[j & 1], ((j >> 1) - 1) & 1, abort_flag);
+          ok = warp_wait(&kv_empty[(j - 2) % C::NSLOT], ((j - 2) / C::NSLOT) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
         }
