@@ -54,13 +54,20 @@ def kernel_counts(shape):
     dkv = B * Hkv * T * S * d * e
     row = B * H * T * 4
     qf32 = B * H * T * d * 4
-    return {
+    counts = {
         "moda_fwd_tc_kernel": {"flops": 2 * gemm, "bytes": q + 2 * kv + 2 * dkv + q + row},
-        "bwd_delta_kernel": {"flops": 0.0, "bytes": 2 * q + row},
-        "moda_bwd_depth_kernel": {"flops": 0.0, "bytes": 2 * dkv + 2 * q + 2 * row + 2 * dkv + qf32},
+        "bwd_delta_kernel": {"flops": 0.0, "bytes": 2 * q + 3 * row},
+        # with depth slots the depth kernel also forms Delta = dO . O and the row statistics
+        # (reads o and lse, writes {-lse*log2 e, Delta}); there is no separate Delta kernel
+        "moda_bwd_depth_kernel": {"flops": 0.0, "bytes": 4 * dkv + 3 * q + 3 * row + qf32},
         "moda_bwd_dkdv_kernel": {"flops": 4 * gemm, "bytes": 2 * kv + 2 * q + 2 * row + 2 * kv},
         "moda_bwd_dq_kernel": {"flops": 3 * gemm, "bytes": 2 * q + 2 * kv + 2 * row + qf32 + q},
     }
+    if S > 0:
+        del counts["bwd_delta_kernel"]
+    else:
+        del counts["moda_bwd_depth_kernel"]
+    return counts
 
 
 def bytes_moved(shape):
@@ -339,6 +346,8 @@ def main():
     kernel_ms = {"moda_fwd_tc_kernel": fwd_ms}
     for j, name in enumerate(("bwd_delta_kernel", "moda_bwd_depth_kernel", "moda_bwd_dkdv_kernel",
                               "moda_bwd_dq_kernel")):
+        if (name == "bwd_delta_kernel") != (shape.S == 0):
+            continue  # with depth slots Delta is formed by the depth kernel; without, there is no depth kernel
         kernel_ms[name] = statistics.mean(ev[i][2 + 2 * j].elapsed_time(ev[i][3 + 2 * j]) for i in range(K))
     status = binding.moda_device_status()
     if status != 0:

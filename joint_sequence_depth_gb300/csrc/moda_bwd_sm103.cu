@@ -44,7 +44,8 @@ struct BwdTcParams {
   float scale, scale_log2;
   const __nv_bfloat16 *q, *k, *v, *kd, *vd, *dout;
   const float* lse;
-  const float2* stats;  // {-lse * log2(e), Delta} per row
+  float2* stats;  // {-lse * log2(e), Delta} per row (written by the depth kernel when S > 0)
+  const __nv_bfloat16* o;  // forward output (Delta = dO . O)
   float* dq_accum;  // depth share of dq, float32 [B,H,T,d] (read by the dQ kernel when S > 0)
   __nv_bfloat16 *dq, *dk, *dv, *dkd, *dvd;
   int* status;
@@ -55,7 +56,8 @@ struct BwdTcParams {
 // a warp step covers SPW = 32 / (d/8) consecutive slots, each slot row read with one
 // coalesced 16-byte load per lane.  The G heads of the position (HG >= G) stay in
 // registers (q, dO packed bf16), so each depth element is read from HBM once and used
-// for all G heads.
+// for all G heads.  The warp also forms the row statistics of its G rows,
+// {-lse * log2(e), Delta = dO . O}, and stores them for the dK/dV and dQ kernels.
 template <int D, int HG>
 __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p) {
   constexpr int CH = D / 8;
@@ -68,20 +70,6 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
   const int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
   const int j = lane / CH, cc = lane % CH;
 
-  uint4 qv[HG], dv4[HG];
-  float lse2[HG], dl[HG], dq[HG][8];
-#pragma unroll
-  for (int hh = 0; hh < HG; ++hh) {
-    const bool hv = hh < p.G;
-    const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + (hv ? hh : 0)) * p.T + t;
-    qv[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.q + row * D) + cc) : make_uint4(0, 0, 0, 0);
-    dv4[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.dout + row * D) + cc) : make_uint4(0, 0, 0, 0);
-    const float2 st = hv ? p.stats[row] : make_float2(-INFINITY, 0.f);
-    lse2[hh] = -st.x;
-    dl[hh] = st.y;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
-  }
   const int64_t slab = pid * p.S * D;
   auto load_slot = [&](int i, uint4& kv, uint4& vv) {
     const bool sv = i < p.S;
@@ -90,8 +78,38 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
     vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
             : make_uint4(0, 0, 0, 0);
   };
-  uint4 kn, vn;  // next step's slot rows, loaded one step ahead
+  uint4 kn, vn;  // next step's slot rows, loaded one step ahead (issued before the row loads)
   load_slot(j, kn, vn);
+  uint4 qv[HG], dv4[HG], ov[HG];
+  float lse2[HG], dl[HG], dq[HG][8];
+  int64_t rows[HG];
+#pragma unroll
+  for (int hh = 0; hh < HG; ++hh) {  // all row loads first, then the dependent arithmetic
+    const bool hv = hh < p.G;
+    rows[hh] = (static_cast<int64_t>(b) * p.H + g * p.G + (hv ? hh : 0)) * p.T + t;
+    qv[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.q + rows[hh] * D) + cc) : make_uint4(0, 0, 0, 0);
+    dv4[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.dout + rows[hh] * D) + cc) : make_uint4(0, 0, 0, 0);
+    ov[hh] = hv ? __ldg(reinterpret_cast<const uint4*>(p.o + rows[hh] * D) + cc) : make_uint4(0, 0, 0, 0);
+    lse2[hh] = hv ? __ldg(p.lse + rows[hh]) * kLog2e : INFINITY;
+  }
+#pragma unroll
+  for (int hh = 0; hh < HG; ++hh) {
+    float dsum = dot2_bf16(dv4[hh].x, ov[hh].x, 0.f);
+    dsum = dot2_bf16(dv4[hh].y, ov[hh].y, dsum);
+    dsum = dot2_bf16(dv4[hh].z, ov[hh].z, dsum);
+    dsum = dot2_bf16(dv4[hh].w, ov[hh].w, dsum);
+    dl[hh] = dsum;
+  }
+#pragma unroll
+  for (int off = CH / 2; off >= 1; off >>= 1)
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) dl[hh] += __shfl_xor_sync(0xffffffffu, dl[hh], off);
+#pragma unroll
+  for (int hh = 0; hh < HG; ++hh) {
+    if (hh < p.G && lane == 0) p.stats[rows[hh]] = make_float2(-lse2[hh], dl[hh]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
+  }
   for (int i0 = 0; i0 < p.S; i0 += SPW) {
     const int i = i0 + j;
     const bool sv = i < p.S;
@@ -1473,6 +1491,7 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.lse = a.lse;
   p.stats = a.stats;
+  p.o = static_cast<const __nv_bfloat16*>(a.o);
   p.dq_accum = a.dq_accum;
   p.dq = static_cast<__nv_bfloat16*>(a.dq);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -1481,11 +1500,15 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.dvd = static_cast<__nv_bfloat16*>(a.dvd);
   p.status = a.status;
 
-  // stage 0: Delta; stage 1: depth gradients; stage 2: dK/dV; stage 3: dQ (needs stage 1's
-  // depth share of dQ).
+  // stage 0: Delta (its own kernel only when S = 0; otherwise the depth kernel forms the
+  // row statistics); stage 1: depth gradients; stage 2: dK/dV; stage 3: dQ (needs stage
+  // 1's depth share of dQ).
+  cudaError_t e = cudaSuccess;
   mark_event(a, 0, s);
-  cudaError_t e = launch_bwd_delta(a, 1, s);
-  if (e != cudaSuccess) return e;
+  if (pr.S == 0) {
+    e = launch_bwd_delta(a, 1, s);
+    if (e != cudaSuccess) return e;
+  }
   mark_event(a, 1, s);
   const int64_t positions = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;
   mark_event(a, 2, s);
