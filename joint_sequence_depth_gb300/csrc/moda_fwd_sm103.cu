@@ -307,14 +307,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
         mma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int t, int item, bool acc) {
+      // pv_done is committed only after a tile's last PV of the unit (for its epilogue):
+      // before that, S of the next key tile, issued after this PV, tells the softmax warps
+      // that O is up to date (MMAs of one thread complete in order).
+      auto issue_pv = [&](int t, int item, bool acc, bool last) {
         const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
         const uint32_t p_tmem = tmem + C::tm_p(t);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts(tmem + C::tm_o(t), p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
                       (acc || kk > 0) ? 1u : 0u);
-        mma_commit(&pv_done[t]);
+        if (last) mma_commit(&pv_done[t]);
       };
       // The issuing thread is on the critical path between MMA groups: item indices are
       // kept incremental, and the depth and sequence steps have a loop each.
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++pcnt0;
           tc_fence_after();
-          issue_pv(0, va, i > 0);
+          issue_pv(0, va, i > 0, i + 1 == nA);
           if (!wait_item(ka)) {
             ok = false;
             break;
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++pcnt1;
             tc_fence_after();
-            issue_pv(1, vb, i > 0);
+            issue_pv(1, vb, i > 0, i + 1 == nB);
             release(vb);
           }
           release(va);
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++pcnt0;
             tc_fence_after();
-            issue_pv(0, iv, !first);
+            issue_pv(0, iv, !first, j + 1 == mA);
           }
           const bool next = j + 1 < m;
           if (next && !wait_item(ik)) {
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++pcnt1;
             tc_fence_after();
-            issue_pv(1, iv, !first);
+            issue_pv(1, iv, !first, j + 1 == mB);
           }
           release(iv);  // V_j: every PV reading it is issued
           if (j + 1 < mB) {
@@ -594,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wp_lo = (wq * 32) / p.G, wp_hi = min(wq * 32 + 31, p.P * p.G - 1) / p.G;
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, jcnt = 0;  // s_full phases consumed, PVs of this tile so far
+    uint32_t ucnt = 0;            // units with keys for this tile so far (pv_done phases, d = 128)
     bool ok = true;
     for (int k = 0; ok && k < n_c; ++k) {
       const Unit u = unit_at(p, cta, k);
@@ -686,33 +690,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run *= corr;
             m_run = m_new;
           }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          // P of the whole tile into registers first: only its store has to wait for the
+          // previous PV of this tile to have read P_t
+          uint32_t pk[BN / 2];
+#pragma unroll
+          for (int c = 0; c < BN; c += 4) {
+            float x0, x1, x2, x3;
+            ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
+            ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+            x2 = ex2(x2);
+            x3 = ex2(x3);
+            if ((c & 4) == 0)
+              fadd2(ls0, ls1, x0, x1), fadd2(ls0, ls1, x2, x3);
+            else
+              fadd2(ls2, ls3, x0, x1), fadd2(ls2, ls3, x2, x3);
+            pk[c >> 1] = pack_bf16(x0, x1);
+            pk[(c >> 1) + 1] = pack_bf16(x2, x3);
+          }
           if (!pv_waited) {
             ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
           }
-          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = half * 64; c < half * 64 + 64; c += 4) {
-              float x0, x1, x2, x3;
-              ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
-              ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
-              x0 = ex2(x0);
-              x1 = ex2(x1);
-              x2 = ex2(x2);
-              x3 = ex2(x3);
-              if ((c & 4) == 0)
-                fadd2(ls0, ls1, x0, x1), fadd2(ls0, ls1, x2, x3);
-              else
-                fadd2(ls2, ls3, x0, x1), fadd2(ls2, ls3, x2, x3);
-              pk[(c - half * 64) >> 1] = pack_bf16(x0, x1);
-              pk[((c - half * 64) >> 1) + 1] = pack_bf16(x2, x3);
-            }
-            tmem_st32(p_tmem + half * 32, pk);
-          }
+          tmem_st64(p_tmem, pk);
         } else {
         // Two halves of 64 keys.  P of the first half is written (over S columns already
         // read) before the second half is loaded; if the second half raises the running max
@@ -744,10 +747,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float corr = (m_run == -INFINITY || !need) ? 1.f : ex2(m_run - m_new);
             if (__any_sync(0xffffffffu, corr != 1.f)) {
               if (j > 0) {
-                // the previous PV of this tile must have landed in O before it is rescaled
-                ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
+                // the previous PV of this tile has landed in O: S of this step, issued after
+                // it, is complete
 #pragma unroll 1
                 for (int c = 0; c < D / 16; ++c) {
                   uint32_t o[16];
@@ -802,8 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
       if (n_t > 0) {
-        ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+        ok = warp_wait(&pv_done[t], (C::SPLIT ? jcnt - 1 : ucnt) & 1, abort_flag);
         if (!ok) break;
+        ++ucnt;
         tc_fence_after();
         const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
         const int h = u.g * p.G + hl;
