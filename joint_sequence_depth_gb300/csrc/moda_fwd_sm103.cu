@@ -73,9 +73,13 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2],
-  // o_free[2], s_free[2], drain[2]
-  static constexpr int NBAR = 2 * NSLOT + 16;
+  // kv_full[2 * NSLOT], kv_empty[NSLOT], q_full[2], q_empty[2], s_full[2], p_full[2],
+  // pv_done[2], o_free[2], s_free[2], drain[2].  Each ring slot has two full barriers, used
+  // by its even and odd loads: with one issuer per query tile an issuer can reach an item
+  // whose slot still holds, not yet landed, an item only the other tile reads; the barrier
+  // of its own item was last used two loads earlier, by a load every reader has consumed
+  // (and so completed), so its parity wait cannot pass on an older load.
+  static constexpr int NBAR = 3 * NSLOT + 16;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
   static_assert(SMEM <= kSmemLimit, "shared memory");
   // TMEM columns.  SPLIT (d = 64): S_t, P_t, O_t of tile t each in columns of their own,
@@ -168,9 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_c = units_of_cta(p, cta);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + C::NSLOT;
-  uint64_t* q_full = bars + 2 * C::NSLOT;
+  uint64_t* kv_full = bars;  // [2 * NSLOT]: slot s, load generation g -> kv_full[2s + (g & 1)]
+  uint64_t* kv_empty = bars + 2 * C::NSLOT;
+  uint64_t* q_full = bars + 3 * C::NSLOT;
   uint64_t* q_empty = q_full + 2;
   uint64_t* s_full = q_empty + 2;
   uint64_t* p_full = s_full + 2;
@@ -184,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_full[2 * i], 1);
+      mbar_init(&kv_full[2 * i + 1], 1);
       mbar_init(&kv_empty[i], C::SPLIT ? 2 : 1);  // released by each MMA issuer
     }
     for (int t = 0; t < 2; ++t) {
@@ -250,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* dst = smem + C::OFF_KV + slot * C::TILE_BYTES;
-          mbar_arrive_expect_tx(&kv_full[slot], C::TILE_BYTES);
+          uint64_t* full = &kv_full[2 * slot + (use & 1)];
+          mbar_arrive_expect_tx(full, C::TILE_BYTES);
           if (r < u.nd_items) {
             // depth step i: K of each query tile, then V of each
             const int i = r / (2 * two), w = r % (2 * two);
@@ -258,13 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = (u.bg * p.T + u.p0 + t * p.P) * p.S + i * BN;
             const CUtensorMap* map = kind ? &tmVd : &tmKd;
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * (BN * 128), map, &kv_full[slot], h * 64, row);
+            for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * (BN * 128), map, full, h * 64, row);
           } else {
             const int j = (r - u.nd_items) >> 1, kind = (r - u.nd_items) & 1;
             const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
             for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(dst + h * (BN * 128), map, &kv_full[slot], h * 64, j * BN, u.bg);
+              tma_load_3d(dst + h * (BN * 128), map, full, h * 64, j * BN, u.bg);
           }
           issued = it + 1;
         }
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let every copy still in flight land before the CTA exits
         volatile int never = 0;
         for (int i = max(0, issued - C::NSLOT); i < issued; ++i)
-          mbar_wait(&kv_full[i % C::NSLOT], (i / C::NSLOT) & 1, &never);
+          mbar_wait(&kv_full[2 * (i % C::NSLOT) + ((i / C::NSLOT) & 1)], (i / C::NSLOT / 2) & 1, &never);
         if (q_issued0 > 0) mbar_wait(&q_full[0], (q_issued0 - 1) & 1, &never);
         if (q_issued1 > 0) mbar_wait(&q_full[1], (q_issued1 - 1) & 1, &never);
       }
@@ -293,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pcnt0 = 0, pcnt1 = 0;  // p_full phases consumed per tile
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
-        return mbar_wait(&kv_full[item % C::NSLOT], (item / C::NSLOT) & 1, abort_flag);
+        const int g = item / C::NSLOT;  // load generation of the slot
+        return mbar_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
       };
       auto release = [&](int item) { mma_commit(&kv_empty[item % C::NSLOT]); };
       static_assert((C::NSLOT & (C::NSLOT - 1)) == 0, "ring size");
@@ -472,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t scnt = 0, pcnt = 0;      // S issued, p_full phases consumed
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
-        return mbar_wait(&kv_full[item % C::NSLOT], (item / C::NSLOT) & 1, abort_flag);
+        const int g = item / C::NSLOT;  // load generation of the slot
+        return mbar_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
       };
       auto release = [&](int item, bool shared) {
         mma_commit(&kv_empty[item % C::NSLOT]);
