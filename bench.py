@@ -42,6 +42,12 @@ def flops(shape):
             "bwd_depth": 2.5 * depth, "bwd": 2.5 * (seq + depth)}
 
 
+def bwd_kernel_name(kind, d):
+    """Name of the tensor-core backward kernel of `kind` ("dkdv" or "dq") for head size d
+    (the d = 64 kernels use 128-wide tiles and have kernels of their own)."""
+    return f"moda_bwd_{kind}64_kernel" if d == 64 else f"moda_bwd_{kind}_kernel"
+
+
 def kernel_counts(shape):
     """Algorithmic FLOPs (tensor-core contractions over the causal triangle; one GEMM is
     2*B*H*d*T(T+1)/2) and HBM bytes (each tensor read or written once) per launch of each
@@ -60,8 +66,8 @@ def kernel_counts(shape):
         # with depth slots the depth kernel also forms Delta = dO . O and the row statistics
         # (reads o and lse, writes {-lse*log2 e, Delta}); there is no separate Delta kernel
         "moda_bwd_depth_kernel": {"flops": 0.0, "bytes": 4 * dkv + 3 * q + 3 * row + qf32},
-        "moda_bwd_dkdv_kernel": {"flops": 4 * gemm, "bytes": 2 * kv + 2 * q + 2 * row + 2 * kv},
-        "moda_bwd_dq_kernel": {"flops": 3 * gemm, "bytes": 2 * q + 2 * kv + 2 * row + qf32 + q},
+        bwd_kernel_name("dkdv", d): {"flops": 4 * gemm, "bytes": 2 * kv + 2 * q + 2 * row + 2 * kv},
+        bwd_kernel_name("dq", d): {"flops": 3 * gemm, "bytes": 2 * q + 2 * kv + 2 * row + qf32 + q},
     }
     if S > 0:
         del counts["bwd_delta_kernel"]
@@ -113,7 +119,9 @@ KERNEL_SOURCES = {"moda_fwd_tc_kernel": ["moda_fwd_sm103.cu", "sm103_ptx.cuh"],
                   "bwd_delta_kernel": ["moda_simt.cu"],
                   "moda_bwd_depth_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
                   "moda_bwd_dkdv_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
-                  "moda_bwd_dq_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"]}
+                  "moda_bwd_dq_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_bwd_dkdv64_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_bwd_dq64_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"]}
 
 
 def source_digest(kernel):
@@ -344,8 +352,8 @@ def main():
     fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
     bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][9]) for i in range(K))
     kernel_ms = {"moda_fwd_tc_kernel": fwd_ms}
-    for j, name in enumerate(("bwd_delta_kernel", "moda_bwd_depth_kernel", "moda_bwd_dkdv_kernel",
-                              "moda_bwd_dq_kernel")):
+    for j, name in enumerate(("bwd_delta_kernel", "moda_bwd_depth_kernel", bwd_kernel_name("dkdv", shape.d),
+                              bwd_kernel_name("dq", shape.d))):
         if (name == "bwd_delta_kernel") != (shape.S == 0):
             continue  # with depth slots Delta is formed by the depth kernel; without, there is no depth kernel
         kernel_ms[name] = statistics.mean(ev[i][2 + 2 * j].elapsed_time(ev[i][3 + 2 * j]) for i in range(K))

@@ -29,6 +29,11 @@ SMALL = [
     ("bf16_no_depth", 1, 4, 2, 257, 64, 0, bf16),
     ("bf16_t1", 1, 4, 2, 1, 64, 2, bf16),
     ("bf16_t9", 1, 2, 1, 9, 128, 1, bf16),
+    # d = 64 tensor-core kernels (128-wide tiles): G = 3 leaves 2 padding rows per tile,
+    # G = 8, and more CTAs than SMs
+    ("bf16_d64_g3_ragged", 1, 6, 2, 300, 64, 5, bf16),
+    ("bf16_d64_g8", 1, 16, 2, 260, 64, 3, bf16),
+    ("bf16_d64_g1_ctas_gt_sms", 2, 16, 16, 700, 64, 4, bf16),
 ]
 
 

@@ -35,6 +35,11 @@ SMALL = [
     ("bf16_g8", 1, 16, 2, 200, 128, 2, bf16),
     ("bf16_one_slot_long", 1, 4, 1, 1024, 128, 1, bf16),
     ("bf16_g16_d64", 1, 16, 1, 130, 64, 4, bf16),
+    # more work units than SMs, so a CTA runs several; the last unit of every (b, kv head)
+    # has an empty second query tile (T is not a multiple of the unit's two tiles)
+    ("bf16_d64_g1_units_gt_sms", 2, 16, 16, 1100, 64, 4, bf16),
+    ("bf16_d64_g4_units_gt_sms", 3, 16, 4, 1100, 64, 8, bf16),
+    ("bf16_d128_g1_units_gt_sms", 2, 16, 16, 1100, 128, 4, bf16),
 ]
 
 
