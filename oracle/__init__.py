@@ -11,6 +11,7 @@ from .oracle import (  # noqa: F401
     backward,
     backward_positions,
     backward_keys,
+    decode,
     DTYPE_F64,
     DTYPE_F32,
     DTYPE_BF16,

@@ -194,3 +194,51 @@ def backward(q, k, v, kd, vd, dout, scale=None, seq_window=0, nthreads=0):
     dq = dqp.reshape(B, Hkv, T, G, d).transpose(0, 1, 3, 2, 4).reshape(B, H, T, d)
     return (dq, dk.reshape(B, Hkv, T, d), dv.reshape(B, Hkv, T, d),
             dkd.reshape(B, Hkv, T, S, d), dvd.reshape(B, Hkv, T, S, d))
+
+
+def _widen(a):
+    """Stored values as float64: float64 as is, float32 widened, bf16 (uint16 bit patterns,
+    the upper half of a float32) widened exactly."""
+    a = np.asarray(a)
+    if a.dtype == np.float64:
+        return a
+    if a.dtype == np.float32:
+        return a.astype(np.float64)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(f"unsupported storage type {a.dtype}")
+
+
+def decode(q, k, v, kd, vd, scale=None):
+    """One decode step of the joint operator ("Mixture-of-Depths Attention", frame "One
+    denominator allocates probability across both memories", with the decode cache of the
+    Table 1 frame "Depth compute still accumulates quadratically in depth"): the query of
+    the newest position T-1 attends to every cached sequence key j <= T-1 and to the S depth
+    slots of its own position, under one softmax.
+
+    q[B,H,d], k/v[B,Hkv,T,d] (the sequence cache, newest position included),
+    kd/vd[B,Hkv,S,d] (the depth slots of the newest position) -> (o[B,H,d], lse[B,H]),
+    float64.  Plain definition: gather the scores, subtract the maximum, sum, divide once.
+    """
+    Q, K, V, KD, VD = (_widen(a) for a in (q, k, v, kd, vd))
+    B, H, d = Q.shape
+    Hkv, T = K.shape[1], K.shape[2]
+    S = KD.shape[2]
+    if K.shape != (B, Hkv, T, d) or V.shape != K.shape or KD.shape != (B, Hkv, S, d) or VD.shape != KD.shape:
+        raise ValueError("shape mismatch: q[B,H,d], k/v[B,Hkv,T,d], kd/vd[B,Hkv,S,d]")
+    if H % Hkv or T < 1:
+        raise ValueError("H must be a multiple of Hkv and T >= 1")
+    G = H // Hkv
+    sc = float(scale) if scale else 1.0 / np.sqrt(d)
+    o = np.empty((B, H, d), np.float64)
+    lse = np.empty((B, H), np.float64)
+    for b in range(B):
+        for h in range(H):
+            g = h // G
+            scores = np.concatenate([K[b, g] @ Q[b, h], KD[b, g] @ Q[b, h]]) * sc
+            m = scores.max()
+            e = np.exp(scores - m)
+            z = e.sum()
+            o[b, h] = (e[:T] @ V[b, g] + e[T:] @ VD[b, g]) / z
+            lse[b, h] = m + np.log(z)
+    return o, lse

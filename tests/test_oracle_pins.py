@@ -275,3 +275,56 @@ def test_oracle_exp2_form_equivalence():
     s2 = s * math.log2(math.e)
     base2 = np.exp2(s2 - s2.max()) / np.exp2(s2 - s2.max()).sum()
     np.testing.assert_allclose(base2, nat, rtol=1e-13, atol=0)
+
+
+# ------------------------------------------------------------------ decode
+def test_oracle_decode_is_the_operators_last_row(oracle_mod):
+    """A decode step is the newest row of the joint operator: the C++ oracle's row T-1 of
+    a full problem whose depth slab at T-1 is the decode step's slots."""
+    B, H, Hkv, T, S, d = 2, 6, 2, 37, 5, 16
+    q, k, v, kd, vd = rand_problem(B, H, Hkv, T, S, d, seed=71)
+    rows = np.array([(b * H + h) * T + T - 1 for b in range(B) for h in range(H)], dtype=np.int64)
+    ro, rl = oracle_mod.forward(q, k, v, kd, vd, rows=rows)
+    o, lse = oracle_mod.decode(q[:, :, T - 1], k, v, kd[:, :, T - 1], vd[:, :, T - 1])
+    np.testing.assert_allclose(o.reshape(B * H, d), ro, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.reshape(B * H), rl, rtol=0, atol=1e-12)
+
+
+def test_oracle_decode_no_depth_is_single_query_attention(oracle_mod):
+    """S = 0: softmax attention of one query over all T cached keys (torch SDPA, float64)."""
+    B, H, Hkv, T, d = 1, 4, 2, 23, 8
+    rng = np.random.default_rng(72)
+    q = rng.standard_normal((B, H, d))
+    k = rng.standard_normal((B, Hkv, T, d))
+    v = rng.standard_normal((B, Hkv, T, d))
+    kd = np.zeros((B, Hkv, 0, d))
+    o, lse = oracle_mod.decode(q, k, v, kd, kd)
+    G = H // Hkv
+    kt = torch.from_numpy(k).repeat_interleave(G, dim=1)
+    vt = torch.from_numpy(v).repeat_interleave(G, dim=1)
+    qt = torch.from_numpy(q)[:, :, None, :]
+    ref = F.scaled_dot_product_attention(qt, kt, vt)[:, :, 0]
+    ref_lse = torch.logsumexp(torch.matmul(qt, kt.transpose(-1, -2))[:, :, 0] / math.sqrt(d), dim=-1)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_oracle_decode_brute_force_and_constant_values(oracle_mod):
+    """Tiny case against explicit math.exp loops; constant values give that constant."""
+    rng = np.random.default_rng(73)
+    q = rng.standard_normal((1, 1, 3))
+    k = rng.standard_normal((1, 1, 2, 3))
+    v = rng.standard_normal((1, 1, 2, 3))
+    kd = rng.standard_normal((1, 1, 2, 3))
+    vd = rng.standard_normal((1, 1, 2, 3))
+    o, lse = oracle_mod.decode(q, k, v, kd, vd)
+    sc = 1 / math.sqrt(3)
+    keys = [k[0, 0, 0], k[0, 0, 1], kd[0, 0, 0], kd[0, 0, 1]]
+    vals = [v[0, 0, 0], v[0, 0, 1], vd[0, 0, 0], vd[0, 0, 1]]
+    w = [math.exp(sc * sum(q[0, 0, c] * kk[c] for c in range(3))) for kk in keys]
+    ref = [sum(w[i] * vals[i][c] for i in range(4)) / sum(w) for c in range(3)]
+    np.testing.assert_allclose(o[0, 0], ref, rtol=1e-13)
+    assert abs(lse[0, 0] - math.log(sum(w))) < 1e-13
+    const = np.full_like(v, 2.5)
+    oc, _ = oracle_mod.decode(q, k, const, kd, np.full_like(vd, 2.5))
+    np.testing.assert_allclose(oc, 2.5, rtol=0, atol=1e-14)
