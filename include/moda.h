@@ -110,6 +110,36 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
                               void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream,
                               void** events, int32_t n_events);
 
+/* Decode step (one new token per sequence; "Mixture-of-Depths Attention", the decode
+ * cache of the Table 1 frame "Depth compute still accumulates quadratically in depth",
+ * with the operation above): for every (b, h) the query of the newest position t = T-1
+ * attends to the sequence keys 0 .. T-1 of the cache (itself included) and to the S
+ * depth slots of its own position, under one softmax:
+ *     a_j = scale * q[b,h,:] . k_cache[b,g,j,:]     j = 0 .. T-1
+ *     b_i = scale * q[b,h,:] . kd[b,g,i,:]          i = 0 .. S-1
+ *     o[b,h,:] = (sum_j e^{a_j} v_cache[b,g,j,:] + sum_i e^{b_i} vd[b,g,i,:]) / (sum of the weights)
+ *     lse[b,h] = ln(sum of the weights)
+ * This is row T-1 of moda_fwd for the same inputs.
+ * desc: B, H, Hkv, S, d as for moda_fwd; T = number of cached positions (>= 1);
+ *       dtype must be MODA_DTYPE_BF16 (else MODA_ERR_UNSUPPORTED); G = H/Hkv <= 8.
+ * Layouts (device, bf16, dense row-major):
+ *     q, o                   [B, H, d]
+ *     k_cache, v_cache       [B, Hkv, kv_capacity, d]   (positions 0 .. T-1 are read)
+ *     kd, vd                 [B, Hkv, S, d]            (may be NULL when S == 0)
+ *     lse                    [B, H] float32, natural log (may be NULL)
+ * kv_capacity: positions allocated per (b, kv head) in the cache; 0 means T; it must
+ * be >= T, and B*Hkv*kv_capacity and B*Hkv*S must be below 2^31.
+ * workspace: device scratch of at least moda_decode_workspace_bytes(desc) bytes,
+ * 256-byte aligned (per-split partial softmax states); calls sharing it must not
+ * overlap on the GPU.  Errors as for moda_fwd; MODA_ERR_WORKSPACE when the workspace
+ * is missing or too small.
+ * Runs two kernels: a key-split pass (TMA-staged K/V sub-tiles, float32 scores and
+ * online softmax on the CUDA cores, the depth slots as one more split) and a merge. */
+size_t moda_decode_workspace_bytes(const moda_desc* desc);
+moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* q, const void* k_cache,
+                        const void* v_cache, const void* kd, const void* vd, void* o, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* moda_bwd for callers that cannot allocate device memory (allocator hooks, runtimes
  * with a device-memory budget fixed at start-up, plain-C callers without an
  * allocator).  The paper has no counterpart: this is a library convenience.

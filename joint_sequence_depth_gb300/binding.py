@@ -27,7 +27,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status",
            "moda_status_str",
            "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
-           "moda_bwd_profiled", "moda_selftest_wait_timeout")
+           "moda_bwd_profiled", "moda_selftest_wait_timeout", "moda_decode", "moda_decode_workspace_bytes")
 
 
 class MODAError(RuntimeError):
@@ -76,6 +76,10 @@ def load_library():
             lib.moda_bwd_noalloc_max_workspace_bytes.restype = ctypes.c_size_t
             lib.moda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, p]
             lib.moda_selftest_wait_timeout.restype = ctypes.c_int
+            lib.moda_decode_workspace_bytes.argtypes = [d]
+            lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
+            lib.moda_decode.argtypes = [d, ctypes.c_int64] + [p] * 8 + [ctypes.c_size_t, p]
+            lib.moda_decode.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -194,3 +198,32 @@ def moda_bwd_noalloc(q, k, v, kd, vd, o, lse, dout, grads, scale=None, stream=No
 
 def moda_bwd_noalloc_max_workspace_bytes() -> int:
     return int(load_library().moda_bwd_noalloc_max_workspace_bytes())
+
+
+def moda_decode_workspace_bytes(desc: moda_desc) -> int:
+    return int(load_library().moda_decode_workspace_bytes(ctypes.byref(desc)))
+
+
+def moda_decode(q, k_cache, v_cache, kd, vd, T=None, o=None, lse=None, workspace=None, scale=None, stream=None):
+    """Decode step (moda_decode in include/moda.h): q[B,H,d] of the newest position,
+    k_cache/v_cache[B,Hkv,capacity,d] holding positions 0..T-1 (T defaults to the
+    capacity), kd/vd[B,Hkv,S,d] (the newest position's depth slots, None when S = 0).
+    Returns (o[B,H,d], lse[B,H] float32)."""
+    B, H, d = q.shape
+    Hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    S = kd.shape[2] if kd is not None else 0
+    T = cap if T is None else int(T)
+    desc = make_desc(B, H, Hkv, T, S, d, q.dtype, scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    need = moda_decode_workspace_bytes(desc)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = load_library().moda_decode(ctypes.byref(desc), ctypes.c_int64(cap), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(kd) if S else None, _ptr(vd) if S else None, _ptr(o), _ptr(lse),
+                                    _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_decode")
+    return o, lse

@@ -186,6 +186,48 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
   return finish(e, s);
 }
 
+size_t moda_decode_workspace_bytes(const moda_desc* desc) {
+  if (check_desc(desc) != MODA_OK) return 0;
+  const moda::DecodeSplit sp = moda::decode_split(problem_of(desc));
+  return align256(static_cast<size_t>(sp.n_split) * desc->B * desc->H * (desc->d + 2) * sizeof(float));
+}
+
+moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* q, const void* k_cache,
+                        const void* v_cache, const void* kd, const void* vd, void* o, float* lse, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (desc->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
+  const int64_t cap = kv_capacity > 0 ? kv_capacity : desc->T;
+  if (cap < desc->T) return MODA_ERR_INVALID_ARG;
+  // TMA row coordinates are 32-bit
+  if (static_cast<int64_t>(desc->B) * desc->Hkv * cap >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(desc->B) * desc->Hkv * desc->S >= (int64_t(1) << 31))
+    return MODA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !o) return MODA_ERR_INVALID_ARG;
+  if (desc->S > 0 && (!kd || !vd)) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {q, k_cache, v_cache, kd, vd, static_cast<const void*>(o), static_cast<const void*>(lse)})
+    if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
+  moda::DecodeArgs a;
+  a.p = problem_of(desc);
+  if (!moda::decode_sm103_supported(a.p)) return MODA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < moda_decode_workspace_bytes(desc)) return MODA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MODA_ERR_INVALID_ARG;
+  a.status = status_word();
+  if (a.status == nullptr) return MODA_ERR_CUDA;
+  a.cap = cap;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.kd = desc->S > 0 ? kd : nullptr;
+  a.vd = desc->S > 0 ? vd : nullptr;
+  a.o = o;
+  a.lse = lse;
+  a.part = static_cast<float*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(moda::launch_decode_sm103(a, s), s);
+}
+
 moda_status moda_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* w = status_word();

@@ -43,6 +43,23 @@ struct BwdArgs {
   int n_events;
 };
 
+// Decode step: q [B,H,d] (the newest position of every head), k/v cache [B,Hkv,cap,d]
+// holding positions 0 .. T-1, kd/vd [B,Hkv,S,d] (the newest position's depth slots).
+struct DecodeArgs {
+  Problem p;
+  int64_t cap;  // positions allocated per (b, kv head) in the cache (>= T)
+  int* status;
+  const void *q, *k, *v, *kd, *vd;
+  void* o;     // [B,H,d]
+  float* lse;  // [B,H], may be null
+  float* part; // workspace: per-split partial states
+};
+struct DecodeSplit {
+  int n_seq;    // sequence splits
+  int chunk;    // sequence keys per split
+  int n_split;  // n_seq (+1 for the depth slots when S > 0)
+};
+
 // Records a.events[k] on `s` when the caller asked for it (profiling only).
 inline void mark_event(const BwdArgs& a, int k, cudaStream_t s) {
   if (a.events != nullptr && k < a.n_events && a.events[k] != nullptr)
@@ -73,6 +90,9 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s)
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_sm103(const BwdArgs& a, cudaStream_t s);
 bool fwd_sm103_supported(const Problem& p);
+DecodeSplit decode_split(const Problem& p);
+bool decode_sm103_supported(const Problem& p);
+cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 bool bwd_sm103_supported(const Problem& p);
 
 }  // namespace moda

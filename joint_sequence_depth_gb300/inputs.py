@@ -88,3 +88,30 @@ def scaled(shape: Shape, **changes) -> Shape:
     fields = dict(shape.__dict__)
     fields.update(changes)
     return Shape(**fields)
+
+
+# Decode steps: one new token per sequence over a cache of T positions (its own included).
+# Shape.T is the number of cached positions; Shape.S the depth slots of the new position.
+DECODE_WORKLOADS = {
+    "bf16_decode_gqa": Shape("bf16_decode_gqa", 8, 32, 8, 32768, 128, 48, torch.bfloat16),
+    "bf16_decode_mha": Shape("bf16_decode_mha", 4, 32, 32, 16384, 128, 8, torch.bfloat16),
+    "bf16_decode_d64": Shape("bf16_decode_d64", 16, 16, 4, 32768, 64, 32, torch.bfloat16),
+}
+DECODE_SEEDS = {name: 101 + i for i, name in enumerate(DECODE_WORKLOADS)}
+
+
+def make_decode_inputs(shape: Shape, seed: int, device="cpu", capacity: int | None = None):
+    """Draw a decode step's q [B,H,d], k/v cache [B,Hkv,capacity,d] (capacity >= T; the
+    positions past T are drawn too and must not influence the step) and kd/vd [B,Hkv,S,d],
+    i.i.d. N(0, 1) in float32 in that order, rounded to the storage type."""
+    cap = capacity or shape.T
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    B, H, Hkv, d, S = shape.B, shape.H, shape.Hkv, shape.d, shape.S
+    dims = {"q": (B, H, d), "k": (B, Hkv, cap, d), "v": (B, Hkv, cap, d), "kd": (B, Hkv, S, d), "vd": (B, Hkv, S, d)}
+    out = {}
+    for key, shp in dims.items():
+        x = torch.randn(shp, generator=gen, device=device, dtype=torch.float32)
+        out[key] = x if shape.dtype == torch.float32 else x.to(shape.dtype)
+        del x
+    return out
