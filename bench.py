@@ -285,10 +285,167 @@ def workload_config(shape):
             "l2": "inputs larger than L2 (no flush)"}
 
 
+DECODE_METRIC = "MoDA decode step GB/s and fraction of the HBM roofline, 1\u00d7GB300"
+
+
+def decode_bytes(shape):
+    """Algorithmic HBM bytes of one decode step: the sequence cache (K, V) and the depth
+    slots read once for the G heads of their kv head, q read, o and lse written."""
+    e = 2
+    B, H, Hkv, T, d, S = shape.B, shape.H, shape.Hkv, shape.T, shape.d, shape.S
+    return 2 * B * Hkv * T * d * e + 2 * B * Hkv * S * d * e + 2 * B * H * d * e + 4 * B * H
+
+
+def decode_config(shape):
+    return {"workload": f"{shape.name}: B={shape.B} H={shape.H} Hkv={shape.Hkv} cached T={shape.T} d={shape.d} "
+                        f"S={shape.S} {shape.dtype_name}, one decode step",
+            "global_batch": shape.B, "seq_len": shape.T, "depth_slots": shape.S,
+            "l2": "K/V cache larger than L2 (no flush)"}
+
+
+def time_oracle_decode(shape, groups):
+    """The float64 oracle on `groups` (batch, kv head) groups of the decode step."""
+    import numpy as np
+    import oracle
+    import torch
+    from joint_sequence_depth_gb300.inputs import DECODE_SEEDS, Shape, make_decode_inputs
+
+    sub = Shape(shape.name, 1, shape.G, 1, shape.T, shape.d, shape.S, shape.dtype)
+    x = make_decode_inputs(sub, seed=DECODE_SEEDS[shape.name])
+    host = [x[n].view(torch.int16).numpy().view(np.uint16) for n in ("q", "k", "v", "kd", "vd")]
+    t0 = time.perf_counter()
+    for _ in range(groups):
+        oracle.decode(*host)
+    per_group = (time.perf_counter() - t0) / groups
+    by = decode_bytes(sub)
+    return {"value": by / per_group / 1e9, "seconds_per_group": per_group, "cores": 1,
+            "sample": f"{groups} (batch, kv head) groups of {shape.G} query heads, T={shape.T}, S={shape.S}, "
+                      f"d={shape.d} ({by / 1e6:.1f} MB each); numpy float64 on one core"}
+
+
+def run_decode(args, shape):
+    """Decode-step benchmark: device time of moda_decode with the cache resident in HBM;
+    e2e adds the step's own inputs (q, kd, vd) from pinned host memory and its outputs
+    (o, lse) back, the cache staying on the device."""
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = max(1, args.steps)
+        r = time_oracle_decode(shape, steps)
+        ms = r["seconds_per_group"] * shape.B * shape.Hkv * 1e3
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": r["value"], "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": steps, "warmup": 0, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": decode_config(shape),
+                "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    import torch.distributed as dist
+
+    from joint_sequence_depth_gb300 import binding
+    from joint_sequence_depth_gb300 import build as mbuild
+    from joint_sequence_depth_gb300.inputs import DECODE_SEEDS, make_decode_inputs
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mbuild.build()
+    binding.load_library()
+    x = make_decode_inputs(shape, seed=DECODE_SEEDS[shape.name] + 1000 * rank, device=dev)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(shape.B, shape.H, dtype=torch.float32, device=dev)
+    desc = binding.make_desc(shape.B, shape.H, shape.Hkv, shape.T, shape.S, shape.d, shape.dtype)
+    ws = torch.empty(binding.moda_decode_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.moda_decode(x["q"], x["k"], x["v"], x["kd"], x["vd"], o=o, lse=lse, workspace=ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    launches0 = binding.moda_launch_count()
+    ev[0].record(stream)
+    for i in range(K):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    launches = binding.moda_launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = ev[0].elapsed_time(ev[K])
+    status = binding.moda_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(status, status)} after the timed steps")
+    # end to end: the step's own inputs in from pinned host memory, outputs back
+    names = ("q", "kd", "vd")
+    host_in = {n: x[n].cpu().pin_memory() for n in names}
+    host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    host_l = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    E = max(3, args.e2e_steps)
+    for _ in range(2):
+        for n in names:
+            x[n].copy_(host_in[n], non_blocking=True)
+        step()
+        host_o.copy_(o, non_blocking=True)
+        host_l.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        for n in names:
+            x[n].copy_(host_in[n], non_blocking=True)
+        step()
+        host_o.copy_(o, non_blocking=True)
+        host_l.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_o.numel() * host_o.element_size() + host_l.numel() * host_l.element_size()
+    ms_per_step, e2e_ms = max_over_ranks([total_ms / K, e2e_ms], dev)
+    by = decode_bytes(shape)
+    value = world * by / (ms_per_step * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    roof = {"bound": "hbm", "achieved": by / (ms_per_step * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": None, "kernel": "moda_decode_kernel (+ moda_decode_merge_kernel)",
+                 "peak_source": f"{peak_kind} (copy)", "algorithmic": {"flops": 0.0, "bytes": by},
+                 "ms": ms_per_step})
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle_decode(shape, 4)
+        cpu = {"value": r["value"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+                "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype_name, "data": "synthetic",
+                "config": decode_config(shape), "clocks": clk,
+                "e2e": {"value": world * by / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
-    from joint_sequence_depth_gb300.inputs import WORKLOADS
+    from joint_sequence_depth_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
 
+    if args.workload in DECODE_WORKLOADS:
+        return run_decode(args, DECODE_WORKLOADS[args.workload])
     base = WORKLOADS[args.workload]
     shape = base
     if args.impl == "reference":
