@@ -12,6 +12,8 @@ from .oracle import (  # noqa: F401
     backward_positions,
     backward_keys,
     decode,
+    depth_store,
+    depth_project,
     DTYPE_F64,
     DTYPE_F32,
     DTYPE_BF16,

@@ -242,3 +242,40 @@ def decode(q, k, v, kd, vd, scale=None):
             o[b, h] = (e[:T] @ V[b, g] + e[T:] @ VD[b, g]) / z
             lse[b, h] = m + np.log(z)
     return o, lse
+
+
+def depth_store(k, v, kd, vd, slot):
+    """Reuse of the attention KV as a depth slot ("Mixture-of-Depths Attention", frame
+    "Reuse attention KV; add a projection for FFN inputs", step 3): the layer's k, v
+    [B,Hkv,T,d] become slot `slot` of kd, vd [B,Hkv,T,S,d]; every other slot is kept.
+    Returns new float64 arrays."""
+    K, V, KD, VD = (_widen(a).copy() for a in (k, v, kd, vd))
+    if K.shape != KD.shape[:3] + KD.shape[4:] or V.shape != K.shape or VD.shape != KD.shape:
+        raise ValueError("shape mismatch: k/v[B,Hkv,T,d], kd/vd[B,Hkv,T,S,d]")
+    if not 0 <= slot < KD.shape[3]:
+        raise ValueError("slot out of range")
+    KD[:, :, :, slot, :] = K
+    VD[:, :, :, slot, :] = V
+    return KD, VD
+
+
+def depth_project(x, wk, wv, kd, vd, slot):
+    """The FFN input projected into an additional depth slot (same frame, step 4):
+    kd[b,g,t,slot,c] = sum_m x[b,t,m] wk[m, g*d + c] and vd likewise with wv, for
+    x[B,T,Dm], wk/wv[Dm, Hkv*d], kd/vd[B,Hkv,T,S,d]; every other slot is kept.
+    A plain float64 matmul per (b); returns new float64 arrays."""
+    X, WK, WV, KD, VD = (_widen(a) for a in (x, wk, wv, kd, vd))
+    KD, VD = KD.copy(), VD.copy()
+    B, T, Dm = X.shape
+    Hkv, S, d = KD.shape[1], KD.shape[3], KD.shape[4]
+    if KD.shape[:3] != (B, Hkv, T) or WK.shape != (Dm, Hkv * d) or WV.shape != WK.shape or VD.shape != KD.shape:
+        raise ValueError("shape mismatch: x[B,T,Dm], wk/wv[Dm,Hkv*d], kd/vd[B,Hkv,T,S,d]")
+    if not 0 <= slot < S:
+        raise ValueError("slot out of range")
+    for b in range(B):
+        pk = X[b] @ WK  # [T, Hkv*d]
+        pv = X[b] @ WV
+        for g in range(Hkv):
+            KD[b, g, :, slot, :] = pk[:, g * d:(g + 1) * d]
+            VD[b, g, :, slot, :] = pv[:, g * d:(g + 1) * d]
+    return KD, VD

@@ -328,3 +328,54 @@ def test_oracle_decode_brute_force_and_constant_values(oracle_mod):
     const = np.full_like(v, 2.5)
     oc, _ = oracle_mod.decode(q, k, const, kd, np.full_like(vd, 2.5))
     np.testing.assert_allclose(oc, 2.5, rtol=0, atol=1e-14)
+
+
+# ------------------------------------------------------------------ depth-KV write path
+def test_oracle_depth_store_places_one_slot(oracle_mod):
+    """The attention KV becomes exactly one slot; the others are untouched."""
+    rng = np.random.default_rng(81)
+    k, v = rng.standard_normal((2, 3, 5, 4)), rng.standard_normal((2, 3, 5, 4))
+    kd, vd = rng.standard_normal((2, 3, 5, 6, 4)), rng.standard_normal((2, 3, 5, 6, 4))
+    nk, nv = oracle_mod.depth_store(k, v, kd, vd, slot=4)
+    np.testing.assert_array_equal(nk[:, :, :, 4], k)
+    np.testing.assert_array_equal(nv[:, :, :, 4], v)
+    others = [s for s in range(6) if s != 4]
+    np.testing.assert_array_equal(nk[:, :, :, others], kd[:, :, :, others])
+    np.testing.assert_array_equal(nv[:, :, :, others], vd[:, :, :, others])
+
+
+def test_oracle_depth_project_brute_force(oracle_mod):
+    """Projection into a slot against explicit sums on a tiny case; other slots kept."""
+    rng = np.random.default_rng(82)
+    B, T, Dm, Hkv, S, d = 2, 3, 5, 2, 3, 4
+    x = rng.standard_normal((B, T, Dm))
+    wk, wv = rng.standard_normal((Dm, Hkv * d)), rng.standard_normal((Dm, Hkv * d))
+    kd, vd = rng.standard_normal((B, Hkv, T, S, d)), rng.standard_normal((B, Hkv, T, S, d))
+    nk, nv = oracle_mod.depth_project(x, wk, wv, kd, vd, slot=1)
+    for b in range(B):
+        for g in range(Hkv):
+            for t in range(T):
+                for c in range(d):
+                    ek = sum(x[b, t, m] * wk[m, g * d + c] for m in range(Dm))
+                    ev = sum(x[b, t, m] * wv[m, g * d + c] for m in range(Dm))
+                    assert abs(nk[b, g, t, 1, c] - ek) < 1e-12 and abs(nv[b, g, t, 1, c] - ev) < 1e-12
+    np.testing.assert_array_equal(nk[:, :, :, [0, 2]], kd[:, :, :, [0, 2]])
+    np.testing.assert_array_equal(nv[:, :, :, [0, 2]], vd[:, :, :, [0, 2]])
+
+
+def test_oracle_depth_project_feeds_the_forward(oracle_mod):
+    """A slot written by the projection is read by the forward as any other slot: with S = 1
+    and the projection of x, the forward equals the forward on a hand-built kd/vd."""
+    rng = np.random.default_rng(83)
+    B, H, Hkv, T, d, Dm = 1, 2, 1, 4, 4, 3
+    q, k, v = rng.standard_normal((B, H, T, d)), rng.standard_normal((B, Hkv, T, d)), rng.standard_normal((B, Hkv, T, d))
+    x = rng.standard_normal((B, T, Dm))
+    wk, wv = rng.standard_normal((Dm, Hkv * d)), rng.standard_normal((Dm, Hkv * d))
+    kd0 = np.zeros((B, Hkv, T, 1, d))
+    nk, nv = oracle_mod.depth_project(x, wk, wv, kd0, kd0, slot=0)
+    hand_k = np.einsum("btm,mc->btc", x, wk).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)[:, :, :, None, :]
+    hand_v = np.einsum("btm,mc->btc", x, wv).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)[:, :, :, None, :]
+    o1, l1 = oracle_mod.forward(q, k, v, nk, nv)
+    o2, l2 = oracle_mod.forward(q, k, v, hand_k, hand_v)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
