@@ -140,6 +140,33 @@ moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* 
                         const void* v_cache, const void* kd, const void* vd, void* o, float* lse, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Depth-KV write path ("Mixture-of-Depths Attention", frame "Reuse attention KV; add a
+ * projection for FFN inputs", Sec. 2.2, and Table 3's KV-projection variants): a layer
+ * writes its contributions to the depth cache that later layers' moda_fwd reads as
+ * kd, vd [B, Hkv, T, S, d], one slot at a time.  Only slot `slot` is written; every
+ * other slot, and every other byte of kd/vd, is left as it was.
+ * desc: B, Hkv, T, S, d as for moda_fwd (H and scale are not used; H must still be a
+ * positive multiple of Hkv); dtype must be MODA_DTYPE_BF16 (else MODA_ERR_UNSUPPORTED);
+ * 0 <= slot < S (else MODA_ERR_INVALID_ARG).  Pointers are device memory, 16-byte
+ * aligned, dense row-major; the caller owns them all.  Launch errors return
+ * MODA_ERR_CUDA; nothing is allocated.
+ *
+ * moda_depth_store_kv: the attention KV reused as a slot:
+ *     kd[b,g,t,slot,:] = k[b,g,t,:],  vd[b,g,t,slot,:] = v[b,g,t,:]
+ * with k, v [B, Hkv, T, d].  One strided-copy kernel (exact). */
+moda_status moda_depth_store_kv(const moda_desc* desc, int32_t slot, const void* k, const void* v, void* kd,
+                                void* vd, void* stream);
+
+/* moda_depth_project_kv: the FFN input projected into a slot:
+ *     kd[b,g,t,slot,c] = sum_m x[b,t,m] * wk[m, g*d + c]
+ *     vd[b,g,t,slot,c] = sum_m x[b,t,m] * wv[m, g*d + c]
+ * with x [B, T, d_model] and wk, wv [d_model, Hkv*d] (bf16).  Products are summed in
+ * float32 on the tensor cores and rounded to bf16 once.  d_model must be a positive
+ * multiple of 8 and Hkv*d a multiple of 64 (else MODA_ERR_INVALID_ARG /
+ * MODA_ERR_UNSUPPORTED).  One GEMM kernel whose epilogue stores straight into the slot. */
+moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d_model, const void* x,
+                                  const void* wk, const void* wv, void* kd, void* vd, void* stream);
+
 /* moda_bwd for callers that cannot allocate device memory (allocator hooks, runtimes
  * with a device-memory budget fixed at start-up, plain-C callers without an
  * allocator).  The paper has no counterpart: this is a library convenience.

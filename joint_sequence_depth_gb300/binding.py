@@ -27,7 +27,8 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_status",
            "moda_status_str",
            "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
-           "moda_bwd_profiled", "moda_selftest_wait_timeout", "moda_decode", "moda_decode_workspace_bytes")
+           "moda_bwd_profiled", "moda_selftest_wait_timeout", "moda_decode", "moda_decode_workspace_bytes",
+           "moda_depth_store_kv", "moda_depth_project_kv")
 
 
 class MODAError(RuntimeError):
@@ -79,6 +80,10 @@ def load_library():
             lib.moda_decode_workspace_bytes.argtypes = [d]
             lib.moda_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.moda_decode.argtypes = [d, ctypes.c_int64] + [p] * 8 + [ctypes.c_size_t, p]
+            lib.moda_depth_store_kv.argtypes = [d, ctypes.c_int32] + [p] * 5
+            lib.moda_depth_store_kv.restype = ctypes.c_int
+            lib.moda_depth_project_kv.argtypes = [d, ctypes.c_int32, ctypes.c_int32] + [p] * 6
+            lib.moda_depth_project_kv.restype = ctypes.c_int
             lib.moda_decode.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -227,3 +232,28 @@ def moda_decode(q, k_cache, v_cache, kd, vd, T=None, o=None, lse=None, workspace
     if st != MODA_OK:
         raise MODAError(st, "moda_decode")
     return o, lse
+
+
+def moda_depth_store_kv(k, v, kd, vd, slot, stream=None):
+    """Writes k, v [B,Hkv,T,d] into slot ``slot`` of kd, vd [B,Hkv,T,S,d] in place
+    (moda_depth_store_kv in include/moda.h); returns (kd, vd)."""
+    B, Hkv, T, S, d = kd.shape
+    desc = make_desc(B, Hkv, Hkv, T, S, d, k.dtype, None)
+    st = load_library().moda_depth_store_kv(ctypes.byref(desc), int(slot), _ptr(k), _ptr(v), _ptr(kd), _ptr(vd),
+                                            _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_depth_store_kv")
+    return kd, vd
+
+
+def moda_depth_project_kv(x, wk, wv, kd, vd, slot, stream=None):
+    """Writes x[B,T,Dm] @ wk and x @ wv (wk, wv [Dm, Hkv*d]) into slot ``slot`` of kd, vd
+    [B,Hkv,T,S,d] in place (moda_depth_project_kv in include/moda.h); returns (kd, vd)."""
+    B, Hkv, T, S, d = kd.shape
+    Dm = x.shape[2]
+    desc = make_desc(B, Hkv, Hkv, T, S, d, x.dtype, None)
+    st = load_library().moda_depth_project_kv(ctypes.byref(desc), int(slot), int(Dm), _ptr(x), _ptr(wk), _ptr(wv),
+                                              _ptr(kd), _ptr(vd), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_depth_project_kv")
+    return kd, vd

@@ -228,6 +228,64 @@ moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* 
   return finish(moda::launch_decode_sm103(a, s), s);
 }
 
+moda_status moda_depth_store_kv(const moda_desc* desc, int32_t slot, const void* k, const void* v, void* kd,
+                                void* vd, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (desc->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
+  if (desc->S < 1 || slot < 0 || slot >= desc->S) return MODA_ERR_INVALID_ARG;
+  if (!k || !v || !kd || !vd) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {k, v, static_cast<const void*>(kd), static_cast<const void*>(vd)})
+    if (!aligned16(p)) return MODA_ERR_INVALID_ARG;
+  moda::DepthWriteArgs a{};
+  a.B = desc->B;
+  a.Hkv = desc->Hkv;
+  a.T = desc->T;
+  a.S = desc->S;
+  a.d = desc->d;
+  a.slot = slot;
+  a.k = k;
+  a.v = v;
+  a.kd = kd;
+  a.vd = vd;
+  a.status = status_word();
+  if (a.status == nullptr) return MODA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(moda::launch_depth_store_sm103(a, s), s);
+}
+
+moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d_model, const void* x,
+                                  const void* wk, const void* wv, void* kd, void* vd, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (desc->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
+  if (desc->S < 1 || slot < 0 || slot >= desc->S) return MODA_ERR_INVALID_ARG;
+  if (d_model < 8 || d_model % 8 != 0) return MODA_ERR_INVALID_ARG;  // 16-byte row strides
+  if ((desc->Hkv * desc->d) % 64 != 0) return MODA_ERR_UNSUPPORTED;
+  if (2LL * desc->B > 65535 || (desc->T + 127) / 128 > 65535) return MODA_ERR_UNSUPPORTED;  // grid limits
+  if (mul_capped(mul_capped(desc->B, desc->T), d_model) > kMaxElems) return MODA_ERR_INVALID_ARG;
+  if (!x || !wk || !wv || !kd || !vd) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {x, wk, wv, static_cast<const void*>(kd), static_cast<const void*>(vd)})
+    if (!aligned16(p)) return MODA_ERR_INVALID_ARG;
+  moda::DepthWriteArgs a{};
+  a.B = desc->B;
+  a.Hkv = desc->Hkv;
+  a.T = desc->T;
+  a.S = desc->S;
+  a.d = desc->d;
+  a.slot = slot;
+  a.Dm = d_model;
+  a.x = x;
+  a.wk = wk;
+  a.wv = wv;
+  a.kd = kd;
+  a.vd = vd;
+  a.status = status_word();
+  if (a.status == nullptr) return MODA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(moda::launch_depth_project_sm103(a, s), s);
+}
+
 moda_status moda_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* w = status_word();

@@ -60,6 +60,15 @@ struct DecodeSplit {
   int n_split;  // n_seq (+1 for the depth slots when S > 0)
 };
 
+// Depth-KV write path: slot `slot` of kd/vd [B,Hkv,T,S,d] from the attention KV
+// (k/v [B,Hkv,T,d]) or from the projection of x [B,T,Dm] by wk/wv [Dm, Hkv*d].
+struct DepthWriteArgs {
+  int B, Hkv, T, S, d, slot, Dm;
+  int* status;
+  const void *k, *v, *x, *wk, *wv;
+  void *kd, *vd;
+};
+
 // Records a.events[k] on `s` when the caller asked for it (profiling only).
 inline void mark_event(const BwdArgs& a, int k, cudaStream_t s) {
   if (a.events != nullptr && k < a.n_events && a.events[k] != nullptr)
@@ -93,6 +102,8 @@ bool fwd_sm103_supported(const Problem& p);
 DecodeSplit decode_split(const Problem& p);
 bool decode_sm103_supported(const Problem& p);
 cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_depth_store_sm103(const DepthWriteArgs& a, cudaStream_t s);
+cudaError_t launch_depth_project_sm103(const DepthWriteArgs& a, cudaStream_t s);
 bool bwd_sm103_supported(const Problem& p);
 
 }  // namespace moda

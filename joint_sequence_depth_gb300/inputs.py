@@ -115,3 +115,38 @@ def make_decode_inputs(shape: Shape, seed: int, device="cpu", capacity: int | No
         out[key] = x if shape.dtype == torch.float32 else x.to(shape.dtype)
         del x
     return out
+
+
+# Depth-KV writes: one layer's contributions to the depth cache of a workload above.
+# The model width is H * d (the query heads side by side); the projection weights map it
+# to the Hkv * d columns of the depth keys (values).
+WRITE_WORKLOADS = {
+    "bf16_write_train": WORKLOADS["bf16_train"],
+    "bf16_write_gqa": WORKLOADS["bf16_gqa"],
+}
+WRITE_SEEDS = {name: 201 + i for i, name in enumerate(WRITE_WORKLOADS)}
+
+
+def d_model(shape: Shape) -> int:
+    return shape.H * shape.d
+
+
+def make_write_inputs(shape: Shape, seed: int, device="cpu", Dm: int | None = None):
+    """Draw k, v [B,Hkv,T,d], kd, vd [B,Hkv,T,S,d], x [B,T,Dm] (Dm defaults to H*d) and
+    wk, wv [Dm, Hkv*d], in that order, i.i.d. N(0, 1) in float32; the weights are then
+    divided by sqrt(Dm) so that projected values have unit variance like the rest; all
+    are rounded to the storage type."""
+    Dm = Dm or d_model(shape)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    B, Hkv, T, d, S = shape.B, shape.Hkv, shape.T, shape.d, shape.S
+    dims = {"k": (B, Hkv, T, d), "v": (B, Hkv, T, d), "kd": (B, Hkv, T, S, d), "vd": (B, Hkv, T, S, d),
+            "x": (B, T, Dm), "wk": (Dm, Hkv * d), "wv": (Dm, Hkv * d)}
+    out = {}
+    for key, shp in dims.items():
+        x = torch.randn(shp, generator=gen, device=device, dtype=torch.float32)
+        if key in ("wk", "wv"):
+            x = x / float(Dm) ** 0.5
+        out[key] = x if shape.dtype == torch.float32 else x.to(shape.dtype)
+        del x
+    return out
