@@ -121,7 +121,9 @@ KERNEL_SOURCES = {"moda_fwd_tc_kernel": ["moda_fwd_sm103.cu", "sm103_ptx.cuh"],
                   "moda_bwd_dkdv_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
                   "moda_bwd_dq_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
                   "moda_bwd_dkdv64_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
-                  "moda_bwd_dq64_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"]}
+                  "moda_bwd_dq64_kernel": ["moda_bwd_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_depth_project_kernel": ["moda_depth_write_sm103.cu", "sm103_ptx.cuh"],
+                  "moda_depth_store_kernel": ["moda_depth_write_sm103.cu"]}
 
 
 def source_digest(kernel):
@@ -440,12 +442,198 @@ def run_decode(args, shape):
     return 0
 
 
+WRITE_METRIC = "MoDA depth-KV write (slot store + FFN-input projection) TFLOP/s and fraction of roofline, 1\u00d7GB300"
+
+
+def write_counts(shape):
+    """Algorithmic work of one layer's depth-KV write: the attention K, V copied into one
+    slot, and x [B,T,Dm] projected by wk, wv [Dm,Hkv*d] into another."""
+    from joint_sequence_depth_gb300.inputs import d_model
+
+    e = 2
+    B, Hkv, T, d = shape.B, shape.Hkv, shape.T, shape.d
+    Dm = d_model(shape)
+    n = Hkv * d
+    return {"flops": 2.0 * 2 * B * T * Dm * n,
+            "store_bytes": 4.0 * B * Hkv * T * d * e,
+            "project_bytes": float(B * T * Dm * e + 2 * Dm * n * e + 2 * B * T * n * e)}
+
+
+def write_config(shape):
+    from joint_sequence_depth_gb300.inputs import d_model
+
+    return {"workload": f"{shape.name}: B={shape.B} Hkv={shape.Hkv} T={shape.T} d={shape.d} S={shape.S} "
+                        f"d_model={d_model(shape)} {shape.dtype_name}, one layer's depth-KV write "
+                        f"(store into slot S-1, projection into slot S/2)",
+            "global_batch": shape.B, "seq_len": shape.T, "depth_slots": shape.S,
+            "l2": "L2 flushed between steps (256 MiB write, then 256 MiB read, outside the timed events)"}
+
+
+def time_oracle_write(shape, T_sample, steps):
+    """The float64 oracle's store + projection on batch 0, positions 0..T_sample-1."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from joint_sequence_depth_gb300.inputs import WRITE_SEEDS, make_write_inputs, scaled
+
+    sub = scaled(shape, B=1, T=T_sample)
+    x = make_write_inputs(sub, seed=WRITE_SEEDS[shape.name])
+    h = {n: t.view(torch.int16).numpy().view(np.uint16) for n, t in x.items()}
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.depth_store(h["k"], h["v"], h["kd"], h["vd"], shape.S - 1)
+        oracle.depth_project(h["x"], h["wk"], h["wv"], h["kd"], h["vd"], shape.S // 2)
+    per = (time.perf_counter() - t0) / steps
+    f = write_counts(sub)["flops"]
+    return {"value": f / per / 1e12, "seconds_per_step": per, "cores": os.cpu_count() or 1,
+            "sample": f"batch 0, positions 0..{T_sample - 1}, all {shape.Hkv} kv heads, S={shape.S}: "
+                      f"store + projection ({f / 1e9:.2f} GFLOP); numpy float64, BLAS may use every host core"}
+
+
+def run_write(args, shape):
+    """Depth-KV write benchmark: one step = moda_depth_store_kv + moda_depth_project_kv on
+    device-resident inputs, L2 flushed between steps; e2e adds the layer's own inputs
+    (k, v, x) from pinned host memory and reads back the written slots of the last position."""
+    world, rank, local = dist_setup(args)
+    T_sample = max(128, shape.T // 32)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = max(1, args.steps)
+        r = time_oracle_write(shape, T_sample, steps)
+        ms = r["seconds_per_step"] * shape.B * (shape.T / T_sample) * 1e3
+        line = {"impl": "reference", "metric": WRITE_METRIC, "value": r["value"], "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": steps, "warmup": 0, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": write_config(shape),
+                "cpu_baseline": {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    import torch.distributed as dist
+
+    from joint_sequence_depth_gb300 import binding
+    from joint_sequence_depth_gb300 import build as mbuild
+    from joint_sequence_depth_gb300.inputs import WRITE_SEEDS, make_write_inputs
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mbuild.build()
+    binding.load_library()
+    x = make_write_inputs(shape, seed=WRITE_SEEDS[shape.name] + 1000 * rank, device=dev)
+    S = shape.S
+    slot_store, slot_proj = S - 1, S // 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        # write 256 MiB (evicts the inputs), then read 256 MiB of another buffer so that the
+        # flush's own dirty lines are written back here and not inside the next timed kernel
+        flush.zero_()
+        clean.sum()
+
+    def step():
+        binding.moda_depth_store_kv(x["k"], x["v"], x["kd"], x["vd"], slot_store)
+        binding.moda_depth_project_kv(x["x"], x["wk"], x["wv"], x["kd"], x["vd"], slot_proj)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    launches0 = binding.moda_launch_count()
+    for i in range(K):
+        flush_l2()
+        ev[i][0].record(stream)
+        binding.moda_depth_store_kv(x["k"], x["v"], x["kd"], x["vd"], slot_store)
+        ev[i][1].record(stream)
+        binding.moda_depth_project_kv(x["x"], x["wk"], x["wv"], x["kd"], x["vd"], slot_proj)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    launches = binding.moda_launch_count() - launches0
+    clk = clocks.stop()
+    store_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    proj_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    status = binding.moda_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(status, status)} after the timed steps")
+    names = ("k", "v", "x")
+    host_in = {n: x[n].cpu().pin_memory() for n in names}
+    host_kd = torch.empty(shape.B, shape.Hkv, 2, shape.d, dtype=x["kd"].dtype, pin_memory=True)
+    host_vd = torch.empty_like(host_kd, pin_memory=True)
+    slots = [slot_proj, slot_store]
+
+    def e2e_step():
+        for n in names:
+            x[n].copy_(host_in[n], non_blocking=True)
+        step()
+        host_kd.copy_(x["kd"][:, :, shape.T - 1, slots], non_blocking=True)
+        host_vd.copy_(x["vd"][:, :, shape.T - 1, slots], non_blocking=True)
+
+    E = max(3, args.e2e_steps)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = 2 * host_kd.numel() * host_kd.element_size()
+    ms_per_step, e2e_ms, proj_ms, store_ms = max_over_ranks([store_ms + proj_ms, e2e_ms, proj_ms, store_ms], dev)
+    c = write_counts(shape)
+    value = world * c["flops"] / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    roof = {"bound": "tensor", "achieved": c["flops"] / (proj_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": traffic_record("moda_depth_project_kernel", shape.name),
+                 "kernel": "moda_depth_project_kernel", "peak_source": f"{peak_kind} bf16 burst (cuBLAS)",
+                 "algorithmic": {"flops": c["flops"], "bytes": c["project_bytes"]}, "ms": proj_ms,
+                 "store_kernel": {"kernel": "moda_depth_store_kernel", "ms": store_ms, "bound": "hbm",
+                                  "achieved": c["store_bytes"] / (store_ms * 1e-3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": c["store_bytes"] / (store_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}})
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle_write(shape, T_sample, 3)
+        cpu = {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+    if rank == 0:
+        line = {"metric": WRITE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+                "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype_name, "data": "synthetic",
+                "config": write_config(shape), "clocks": clk,
+                "e2e": {"value": world * c["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
-    from joint_sequence_depth_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    from joint_sequence_depth_gb300.inputs import DECODE_WORKLOADS, WORKLOADS, WRITE_WORKLOADS
 
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args, DECODE_WORKLOADS[args.workload])
+    if args.workload in WRITE_WORKLOADS:
+        return run_write(args, WRITE_WORKLOADS[args.workload])
     base = WORKLOADS[args.workload]
     shape = base
     if args.impl == "reference":

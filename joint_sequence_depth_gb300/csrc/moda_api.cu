@@ -262,7 +262,7 @@ moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d
   if (desc->S < 1 || slot < 0 || slot >= desc->S) return MODA_ERR_INVALID_ARG;
   if (d_model < 8 || d_model % 8 != 0) return MODA_ERR_INVALID_ARG;  // 16-byte row strides
   if ((desc->Hkv * desc->d) % 64 != 0) return MODA_ERR_UNSUPPORTED;
-  if (2LL * desc->B > 65535 || (desc->T + 127) / 128 > 65535) return MODA_ERR_UNSUPPORTED;  // grid limits
+  if (desc->B > 65535 || (desc->T + 127) / 128 > 65535) return MODA_ERR_UNSUPPORTED;  // grid limits
   if (mul_capped(mul_capped(desc->B, desc->T), d_model) > kMaxElems) return MODA_ERR_INVALID_ARG;
   if (!x || !wk || !wv || !kd || !vd) return MODA_ERR_INVALID_ARG;
   for (const void* p : {x, wk, wv, static_cast<const void*>(kd), static_cast<const void*>(vd)})

@@ -8,11 +8,12 @@
 //             vd[b,g,t,slot,c] = sum_m x[b,t,m] wv[m, g*d + c]
 //
 // The store is a strided copy (16-byte vectors).  The projection is a tcgen05 GEMM: one
-// CTA per 128 positions x 128 output columns of one batch row block and one of K or V;
-// x and w tiles arrive by TMA (128-byte swizzle) through a 3-stage ring, one thread issues
-// the MMAs (M = 128, N = 128, K = 16 steps, float32 accumulator in TMEM), and the epilogue
-// rounds to bf16 once and writes the tile straight into the slot with TMA stores through a
-// tensor map whose rows step over the S slots of a position (the slot scatter).
+// CTA per 128 positions x 128 output columns of one batch row, computing K and V together
+// as one N = 256 product (the x tile is loaded once for both); x and the wk, wv tiles
+// arrive by TMA (128-byte swizzle) through a 2-stage ring (two CTAs per SM), one thread
+// issues the MMAs (M = 128, N = 256, K = 16 steps, float32 accumulators in TMEM), and the
+// epilogue rounds to bf16 once and writes the tiles straight into the slot with TMA stores
+// through a tensor map whose rows step over the S slots of a position (the slot scatter).
 //
 // All waits are bounded (sm103_ptx.cuh); a timeout records MODA_ERR_TIMEOUT.
 #include <cudaTypedefs.h>
@@ -37,22 +38,38 @@ __global__ void __launch_bounds__(256) moda_depth_store_kernel(const DepthWriteA
   const uint4* v = static_cast<const uint4*>(a.v);
   uint4* kd = static_cast<uint4*>(a.kd);
   uint4* vd = static_cast<uint4*>(a.vd);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = i / CH, ch = i % CH;
-    const int64_t dst = (row * a.S + a.slot) * CH + ch;
-    kd[dst] = k[i];
-    vd[dst] = v[i];
+  // four vectors of k and four of v in flight per thread before any store
+  constexpr int U = 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n; i0 += U * stride) {
+    uint4 rk[U], rv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n) {
+        rk[u] = __ldcs(k + i);
+        rv[u] = __ldcs(v + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n) {
+        const int64_t dst = (i / CH * a.S + a.slot) * CH + i % CH;
+        kd[dst] = rk[u];
+        vd[dst] = rv[u];
+      }
+    }
   }
 }
 
 // ---------------------------------------------------------------------------- project
 constexpr int PM = 128;  // positions per tile
-constexpr int PN = 128;  // output columns per tile
+constexpr int PN = 128;  // output columns per tile (of K and of V each)
 constexpr int PK = 64;   // reduction step per stage
-constexpr int PSTAGE = 3;
-constexpr int P_A_BYTES = PM * PK * 2;  // x tile, K-major
-constexpr int P_B_BYTES = PK * PN * 2;  // w tile, two [64 x 64] MN-major blocks
+constexpr int PSTAGE = 2;
+constexpr int P_A_BYTES = PM * PK * 2;      // x tile, K-major
+constexpr int P_B_BYTES = 2 * PK * PN * 2;  // wk then wv tile: four [64 x 64] MN-major blocks
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_OFF_BAR = PSTAGE * P_STAGE_BYTES;  // full[PSTAGE], empty[PSTAGE], done
 constexpr int P_SMEM = P_OFF_BAR + (2 * PSTAGE + 1) * 8 + 16;
@@ -70,7 +87,7 @@ struct ProjParams {
   int* status;
 };
 
-// blockIdx: x = column tile, y = position tile, z = 2 * b + (0: K, 1: V)
+// blockIdx: x = column tile, y = position tile, z = b
 __global__ void __launch_bounds__(128, 2)
     moda_depth_project_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWk,
                               const __grid_constant__ CUtensorMap tmWv, const __grid_constant__ CUtensorMap tmKd,
@@ -83,9 +100,7 @@ __global__ void __launch_bounds__(128, 2)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * PN, t0 = blockIdx.y * PM;
-  const int b = blockIdx.z >> 1, which = blockIdx.z & 1;
-  const CUtensorMap* tmW = which ? &tmWv : &tmWk;
-  const CUtensorMap* tmO = which ? &tmVd : &tmKd;
+  const int b = blockIdx.z;
   const int n_k = (p.Dm + PK - 1) / PK;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_OFF_BAR);
@@ -104,7 +119,7 @@ __global__ void __launch_bounds__(128, 2)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, PN);
+    tmem_alloc(tmem_slot, 2 * PN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -116,7 +131,8 @@ __global__ void __launch_bounds__(128, 2)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ loads
     prefetch_tmap(&tmX);
-    prefetch_tmap(tmW);
+    prefetch_tmap(&tmWk);
+    prefetch_tmap(&tmWv);
     int issued = 0;
     for (int ks = 0; ks < n_k; ++ks) {
       const int st = ks % PSTAGE, use = ks / PSTAGE;
@@ -127,8 +143,9 @@ __global__ void __launch_bounds__(128, 2)
       uint8_t* dst = smem + st * P_STAGE_BYTES;
       mbar_arrive_expect_tx(&full[st], P_STAGE_BYTES);
       tma_load_3d(dst, &tmX, &full[st], ks * PK, t0, b);
-      tma_load_2d(dst + P_A_BYTES, tmW, &full[st], n0, ks * PK);
-      tma_load_2d(dst + P_A_BYTES + PK * 128, tmW, &full[st], n0 + 64, ks * PK);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tma_load_2d(dst + P_A_BYTES + c * (PK * 128), c < 2 ? &tmWk : &tmWv, &full[st], n0 + (c & 1) * 64, ks * PK);
       issued = ks + 1;
     }
     if (!ok) {
@@ -140,7 +157,7 @@ __global__ void __launch_bounds__(128, 2)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16(PM, PN, true);  // B (w) is MN-major
+    constexpr uint32_t IDESC = idesc_bf16(PM, 2 * PN, true);  // B ([wk | wv]) is MN-major
     for (int ks = 0; ks < n_k; ++ks) {
       const int st = ks % PSTAGE;
       if (!mbar_wait(&full[st], (ks / PSTAGE) & 1, abort_flag)) {
@@ -170,11 +187,12 @@ __global__ void __launch_bounds__(128, 2)
   if (!fin && threadIdx.x == 0) record_status(p.status, kStatusTimeout);
   const bool good = __syncthreads_and(fin && !*abort_flag);
   if (good) {
-    // thread = row = TMEM lane; stage the bf16 tile in the freed ring (two 64-column SW128 blocks)
+    // thread = row = TMEM lane; stage the bf16 tiles in the freed ring as four 64-column
+    // SW128 blocks: K columns n0.., n0+64.., then V columns n0.., n0+64..
     const int r = threadIdx.x;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < 4; ++half) {
       uint32_t acc[64];
       tmem_ld64(tmem + lane_base + half * 64, acc);
 #pragma unroll
@@ -189,11 +207,12 @@ __global__ void __launch_bounds__(128, 2)
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
-      // each 64-column block is one head's 64 columns: head n / d, columns n % d
+      // each 64-column block is 64 columns of one head: head n / d, columns n % d
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int n = n0 + half * 64;
-        if (n < p.n_total) tma_store_3d(tmO, sbase + half * (PM * 128), n % p.d, t0, b * p.Hkv + n / p.d);
+      for (int half = 0; half < 4; ++half) {
+        const int n = n0 + (half & 1) * 64;
+        if (n < p.n_total)
+          tma_store_3d(half < 2 ? &tmKd : &tmVd, sbase + half * (PM * 128), n % p.d, t0, b * p.Hkv + n / p.d);
       }
       bulk_commit();
       bulk_wait_all();  // the stores have read the staging tile and written the slot
@@ -203,7 +222,7 @@ __global__ void __launch_bounds__(128, 2)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, PN);
+    tmem_dealloc(tmem, 2 * PN);
   }
 }
 
@@ -242,7 +261,7 @@ int dw_sms() {
 
 cudaError_t launch_depth_store_sm103(const DepthWriteArgs& a, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(a.B) * a.Hkv * a.T * (a.d / 8);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 8LL * dw_sms()));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4LL * dw_sms()));  // 4 x 256 threads per SM
   if (a.d == 64)
     moda_depth_store_kernel<64><<<grid, 256, 0, s>>>(a);
   else
@@ -294,7 +313,7 @@ cudaError_t launch_depth_project_sm103(const DepthWriteArgs& a, cudaStream_t s) 
     done = P_SMEM;
   }
   const dim3 grid(static_cast<unsigned>((n_total + PN - 1) / PN), static_cast<unsigned>((a.T + PM - 1) / PM),
-                  static_cast<unsigned>(2 * a.B));
+                  static_cast<unsigned>(a.B));
   moda_depth_project_kernel<<<grid, 128, P_SMEM, s>>>(tx, twk, twv, tkd, tvd, p);
   count_launches(1);
   return cudaGetLastError();

@@ -121,8 +121,8 @@ def make_decode_inputs(shape: Shape, seed: int, device="cpu", capacity: int | No
 # The model width is H * d (the query heads side by side); the projection weights map it
 # to the Hkv * d columns of the depth keys (values).
 WRITE_WORKLOADS = {
-    "bf16_write_train": WORKLOADS["bf16_train"],
-    "bf16_write_gqa": WORKLOADS["bf16_gqa"],
+    "bf16_write_train": scaled(WORKLOADS["bf16_train"], name="bf16_write_train", backward=False),
+    "bf16_write_gqa": scaled(WORKLOADS["bf16_gqa"], name="bf16_write_gqa"),
 }
 WRITE_SEEDS = {name: 201 + i for i, name in enumerate(WRITE_WORKLOADS)}
 
