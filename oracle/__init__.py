@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     decode,
     depth_store,
     depth_project,
+    sliding_window,
     DTYPE_F64,
     DTYPE_F32,
     DTYPE_BF16,

@@ -279,3 +279,20 @@ def depth_project(x, wk, wv, kd, vd, slot):
             KD[b, g, :, slot, :] = pk[:, g * d:(g + 1) * d]
             VD[b, g, :, slot, :] = pv[:, g * d:(g + 1) * d]
     return KD, VD
+
+
+def sliding_window(kd_hist, vd_hist, window):
+    """Bounded slot buffer with a sliding window ("Mixture-of-Depths Attention", closing
+    frame: an S << L slot buffer, sliding window variant): of the slots written so far,
+    in the order they were written (kd_hist, vd_hist [B,Hkv,T,L,d], slot L-1 the newest),
+    a layer reads only the newest `window` ones.  Returns them, oldest first, as float64
+    arrays [B,Hkv,T,min(L, window),d]; the joint forward over them is forward(q, k, v,
+    *sliding_window(...))."""
+    KD, VD = _widen(kd_hist), _widen(vd_hist)
+    if KD.ndim != 5 or VD.shape != KD.shape:
+        raise ValueError("kd_hist/vd_hist must both be [B,Hkv,T,L,d]")
+    if window < 1:
+        raise ValueError("window must be >= 1")
+    L = KD.shape[3]
+    first = max(0, L - window)
+    return KD[:, :, :, first:L].copy(), VD[:, :, :, first:L].copy()

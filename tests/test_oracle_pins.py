@@ -379,3 +379,59 @@ def test_oracle_depth_project_feeds_the_forward(oracle_mod):
     o2, l2 = oracle_mod.forward(q, k, v, hand_k, hand_v)
     np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ bounded slot buffer
+def test_oracle_sliding_window_keeps_the_newest_in_order(oracle_mod):
+    """Marker histories (slot i of kd holds i + position/100, of vd -i): the window of the
+    newest W slots, oldest first; W >= L keeps all of them."""
+    B, Hkv, T, L, d = 1, 2, 3, 5, 4
+    idx = np.arange(L)[None, None, None, :, None] + np.arange(T)[None, None, :, None, None] / 100.0
+    kd = np.broadcast_to(idx, (B, Hkv, T, L, d)).copy()
+    vd = -kd
+    wk, wv = oracle_mod.sliding_window(kd, vd, 3)
+    assert wk.shape == (B, Hkv, T, 3, d)
+    np.testing.assert_array_equal(np.floor(wk[0, 0, 0, :, 0]), [2, 3, 4])
+    np.testing.assert_array_equal(wv, -wk)
+    w1k, _ = oracle_mod.sliding_window(kd, vd, 1)
+    np.testing.assert_array_equal(np.floor(w1k[..., 0, 0]), 4)
+    allk, allv = oracle_mod.sliding_window(kd, vd, 9)
+    np.testing.assert_array_equal(allk, kd)
+    np.testing.assert_array_equal(allv, vd)
+
+
+def test_oracle_forward_does_not_depend_on_slot_order(oracle_mod):
+    """The joint softmax is a sum over its keys, so permuting a position's slots (keys and
+    values together) leaves o and lse unchanged; permuting the keys alone does not."""
+    q, k, v, kd, vd = rand_problem(1, 4, 2, 9, 6, 8, seed=91)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    o1, l1 = oracle_mod.forward(q, k, v, kd, vd)
+    o2, l2 = oracle_mod.forward(q, k, v, kd[:, :, :, perm], vd[:, :, :, perm])
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+    o3, _ = oracle_mod.forward(q, k, v, kd[:, :, :, perm], vd)
+    assert np.max(np.abs(o3 - o1)) > 1e-3
+
+
+@pytest.mark.parametrize("n_writes", [2, 4, 7, 11])
+def test_oracle_ring_buffer_realises_the_window(oracle_mod, n_writes):
+    """A ring of C slots written at w mod C and read over its first min(n, C) slots gives
+    the forward over the sliding window of the last C writes (brute-force ring, tiny case)."""
+    B, H, Hkv, T, d, C = 1, 2, 1, 5, 4, 4
+    rng = np.random.default_rng(92 + n_writes)
+    q, k, v = (rng.standard_normal(s) for s in ((B, H, T, d), (B, Hkv, T, d), (B, Hkv, T, d)))
+    hist_k = rng.standard_normal((B, Hkv, T, n_writes, d))
+    hist_v = rng.standard_normal((B, Hkv, T, n_writes, d))
+    ring_k = np.full((B, Hkv, T, C, d), 7.0)  # finite junk in slots never written
+    ring_v = np.full((B, Hkv, T, C, d), -7.0)
+    for w in range(n_writes):
+        for b in range(B):
+            for g in range(Hkv):
+                for t in range(T):
+                    ring_k[b, g, t, w % C] = hist_k[b, g, t, w]
+                    ring_v[b, g, t, w % C] = hist_v[b, g, t, w]
+    n_read = min(n_writes, C)
+    o_ring, l_ring = oracle_mod.forward(q, k, v, ring_k[:, :, :, :n_read], ring_v[:, :, :, :n_read])
+    o_win, l_win = oracle_mod.forward(q, k, v, *oracle_mod.sliding_window(hist_k, hist_v, C))
+    np.testing.assert_allclose(o_ring, o_win, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_ring, l_win, rtol=0, atol=1e-12)
