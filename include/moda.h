@@ -21,7 +21,8 @@
  * Layouts: every tensor is dense, contiguous and row-major exactly as shaped:
  *     q, o, dout, dq        [B, H,   T, d]
  *     k, v, dk, dv          [B, Hkv, T, d]
- *     kd, vd, dkd, dvd      [B, Hkv, T, S, d]   (the [S, d] slab of one position is contiguous)
+ *     kd, vd, dkd, dvd      [B, Hkv, T, S, d]   (the [S, d] slab of one position is contiguous;
+ *                                               [B, Hkv, T, C, d] with a slot capacity C, below)
  *     lse                   [B, H,   T]         float32, natural log
  * Element type: all of q..vd, o, dout and the gradients share desc->dtype;
  * lse is always float32.  Arithmetic accumulates in float32.
@@ -63,11 +64,24 @@ typedef enum { MODA_DTYPE_F32 = 0, MODA_DTYPE_BF16 = 1 } moda_dtype;
 
 /* Problem description.  B >= 1, H >= 1, Hkv >= 1 with H % Hkv == 0, T >= 1,
  * S >= 0 (S = 0: the depth history H_l is empty), d in {64, 128}.
- * scale <= 0 selects 1/sqrt(d) (the slides' a_j, b_i use 1/sqrt(d)). */
+ * scale <= 0 selects 1/sqrt(d) (the slides' a_j, b_i use 1/sqrt(d)).
+ *
+ * slot_capacity (bounded slot buffer; "Mixture-of-Depths Attention", the closing
+ * frame's S << L slot buffer with a sliding window): 0 means kd/vd hold exactly S
+ * slots per position.  Otherwise kd/vd (and dkd/dvd) are [B, Hkv, T, C, d] with
+ * C = slot_capacity >= S, and only slots 0 .. S-1 of each position are read; the
+ * layer's depth memory is those S slots, in any order (the softmax does not depend on
+ * the order of its keys).  A sliding window of the last C slots written is a ring:
+ * the w-th write goes to slot w mod C (moda_depth_store_kv / moda_depth_project_kv),
+ * and a reader passes S = min(writes so far, C).  The unread slots S .. C-1 get zero
+ * weight; the tensor-core forward multiplies their value rows by that exact zero, so
+ * they must hold finite numbers (zero a new buffer once).  moda_bwd sets dkd/dvd of
+ * the unread slots to zero. */
 typedef struct {
   int32_t B, H, Hkv, T, S, d;
   int32_t dtype; /* moda_dtype */
   float scale;
+  int32_t slot_capacity;
 } moda_desc;
 
 /* Forward (the operation above).
@@ -125,7 +139,8 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
  * Layouts (device, bf16, dense row-major):
  *     q, o                   [B, H, d]
  *     k_cache, v_cache       [B, Hkv, kv_capacity, d]   (positions 0 .. T-1 are read)
- *     kd, vd                 [B, Hkv, S, d]            (may be NULL when S == 0)
+ *     kd, vd                 [B, Hkv, S, d]            (may be NULL when S == 0;
+ *                                                      [B, Hkv, C, d] with a slot capacity C)
  *     lse                    [B, H] float32, natural log (may be NULL)
  * kv_capacity: positions allocated per (b, kv head) in the cache; 0 means T; it must
  * be >= T, and B*Hkv*kv_capacity and B*Hkv*S must be below 2^31.
@@ -147,7 +162,8 @@ moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* 
  * other slot, and every other byte of kd/vd, is left as it was.
  * desc: B, Hkv, T, S, d as for moda_fwd (H and scale are not used; H must still be a
  * positive multiple of Hkv); dtype must be MODA_DTYPE_BF16 (else MODA_ERR_UNSUPPORTED);
- * 0 <= slot < S (else MODA_ERR_INVALID_ARG).  Pointers are device memory, 16-byte
+ * 0 <= slot < C, the slots per position in memory (slot_capacity, or S when that is 0;
+ * else MODA_ERR_INVALID_ARG).  Pointers are device memory, 16-byte
  * aligned, dense row-major; the caller owns them all.  Launch errors return
  * MODA_ERR_CUDA; nothing is allocated.
  *

@@ -39,7 +39,8 @@ class MODAError(RuntimeError):
 
 class moda_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("T", ctypes.c_int32),
-                ("S", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("S", ctypes.c_int32), ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("slot_capacity", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -89,18 +90,33 @@ def load_library():
     return _lib
 
 
-def make_desc(B, H, Hkv, T, S, d, dtype, scale=None) -> moda_desc:
+def make_desc(B, H, Hkv, T, S, d, dtype, scale=None, slot_capacity=0) -> moda_desc:
     return moda_desc(B, H, Hkv, T, S, d, DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype),
-                     float(scale or 0.0))
+                     float(scale or 0.0), int(slot_capacity))
 
 
-def _desc_from(q, k, kd, scale):
+def _slots(kd, slots):
+    """(S read, slot capacity) for a depth tensor whose dim 3 holds the slots in memory:
+    ``slots=None`` reads them all."""
+    if kd is None:
+        return 0, 0
+    cap = kd.shape[3]
+    if slots is None or int(slots) == cap:
+        return cap, 0
+    return int(slots), cap
+
+
+def _desc_from(q, k, kd, scale, slots=None):
     B, H, T, d = q.shape
     Hkv = k.shape[1]
-    S = kd.shape[3] if kd is not None else 0
+    S, cap = _slots(kd, slots)
     if q.dtype not in DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
-    return make_desc(B, H, Hkv, T, S, d, q.dtype, scale)
+    return make_desc(B, H, Hkv, T, S, d, q.dtype, scale, cap)
+
+
+def _mem_slots(desc):
+    return desc.slot_capacity if desc.slot_capacity > 0 else desc.S
 
 
 def _ptr(t):
@@ -121,15 +137,17 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None):
-    """Joint sequence/depth attention forward.  Returns (o [B,H,T,d], lse [B,H,T] float32)."""
-    desc = _desc_from(q, k, kd, scale)
+def moda_fwd(q, k, v, kd, vd, o=None, lse=None, scale=None, stream=None, slots=None):
+    """Joint sequence/depth attention forward.  Returns (o [B,H,T,d], lse [B,H,T] float32).
+    ``slots``: read only slots 0..slots-1 of kd/vd[B,Hkv,T,C,d] (a bounded slot buffer of
+    capacity C, see slot_capacity in include/moda.h); None reads all C."""
+    desc = _desc_from(q, k, kd, scale, slots)
     B, H, T, d = q.shape
     for t, name in ((k, "k"), (v, "v")):
         _check_like(t, q.dtype, (B, desc.Hkv, T, d), name)
     if desc.S:
         for t, name in ((kd, "kd"), (vd, "vd")):
-            _check_like(t, q.dtype, (B, desc.Hkv, T, desc.S, d), name)
+            _check_like(t, q.dtype, (B, desc.Hkv, T, _mem_slots(desc), d), name)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
@@ -145,11 +163,13 @@ def moda_bwd_workspace_bytes(desc: moda_desc) -> int:
     return int(load_library().moda_bwd_workspace_bytes(ctypes.byref(desc)))
 
 
-def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=None, stream=None, events=None):
+def moda_bwd(q, k, v, kd, vd, o, lse, dout, grads=None, workspace=None, scale=None, stream=None, events=None,
+             slots=None):
     """Backward of moda_fwd.  Returns (dq, dk, dv, dkd, dvd) in the input dtype.  ``events``
     (optional list of torch.cuda.Event) are recorded after each internal stage, see
-    moda_bwd_profiled in include/moda.h."""
-    desc = _desc_from(q, k, kd, scale)
+    moda_bwd_profiled in include/moda.h.  ``slots`` as for moda_fwd (dkd/dvd of the
+    unread slots come back as zero)."""
+    desc = _desc_from(q, k, kd, scale, slots)
     if grads is None:
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
                  torch.empty_like(kd) if desc.S else None, torch.empty_like(vd) if desc.S else None)
@@ -186,11 +206,11 @@ def moda_launch_count() -> int:
     return int(load_library().moda_launch_count())
 
 
-def moda_bwd_noalloc(q, k, v, kd, vd, o, lse, dout, grads, scale=None, stream=None):
+def moda_bwd_noalloc(q, k, v, kd, vd, o, lse, dout, grads, scale=None, stream=None, slots=None):
     """moda_bwd without a workspace argument, for callers that cannot allocate device memory:
     the library uses its own fixed device array (see include/moda.h).  ``grads`` must be
     preallocated (dq, dk, dv, dkd, dvd); returns them."""
-    desc = _desc_from(q, k, kd, scale)
+    desc = _desc_from(q, k, kd, scale, slots)
     dq, dk, dv, dkd, dvd = grads
     st = load_library().moda_bwd_noalloc(
         ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None, _ptr(vd) if desc.S else None,
@@ -209,16 +229,18 @@ def moda_decode_workspace_bytes(desc: moda_desc) -> int:
     return int(load_library().moda_decode_workspace_bytes(ctypes.byref(desc)))
 
 
-def moda_decode(q, k_cache, v_cache, kd, vd, T=None, o=None, lse=None, workspace=None, scale=None, stream=None):
+def moda_decode(q, k_cache, v_cache, kd, vd, T=None, o=None, lse=None, workspace=None, scale=None, stream=None,
+                slots=None):
     """Decode step (moda_decode in include/moda.h): q[B,H,d] of the newest position,
     k_cache/v_cache[B,Hkv,capacity,d] holding positions 0..T-1 (T defaults to the
-    capacity), kd/vd[B,Hkv,S,d] (the newest position's depth slots, None when S = 0).
+    capacity), kd/vd[B,Hkv,C,d] (the newest position's depth slots, None when there are
+    none; only slots 0..slots-1 are read when ``slots`` is given).
     Returns (o[B,H,d], lse[B,H] float32)."""
     B, H, d = q.shape
     Hkv, cap = k_cache.shape[1], k_cache.shape[2]
-    S = kd.shape[2] if kd is not None else 0
+    S, slot_cap = (0, 0) if kd is None else _slots(kd.unsqueeze(2), slots)
     T = cap if T is None else int(T)
-    desc = make_desc(B, H, Hkv, T, S, d, q.dtype, scale)
+    desc = make_desc(B, H, Hkv, T, S, d, q.dtype, scale, slot_cap)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:

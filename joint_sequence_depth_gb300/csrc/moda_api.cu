@@ -31,15 +31,19 @@ int64_t mul_capped(int64_t a, int64_t b) {
   return a * b;
 }
 
+// Slots per position in kd/vd memory: slot_capacity when set, else S.
+int64_t slots_in_memory(const moda_desc* d) { return d->slot_capacity > 0 ? d->slot_capacity : d->S; }
+
 moda_status check_desc(const moda_desc* d) {
   if (d == nullptr) return MODA_ERR_INVALID_ARG;
   if (d->B < 1 || d->H < 1 || d->Hkv < 1 || d->T < 1 || d->S < 0 || d->d < 1) return MODA_ERR_INVALID_ARG;
+  if (d->slot_capacity < 0 || (d->slot_capacity > 0 && d->slot_capacity < d->S)) return MODA_ERR_INVALID_ARG;
   if (d->H % d->Hkv != 0) return MODA_ERR_INVALID_ARG;
   if (!(d->scale <= 0.f || std::isfinite(d->scale))) return MODA_ERR_INVALID_ARG;
   if (d->dtype != MODA_DTYPE_F32 && d->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
   if (d->d != 64 && d->d != 128) return MODA_ERR_UNSUPPORTED;
   const int64_t q = mul_capped(mul_capped(mul_capped(d->B, d->H), d->T), d->d);
-  const int64_t kd = mul_capped(mul_capped(mul_capped(mul_capped(d->B, d->Hkv), d->T), d->S), d->d);
+  const int64_t kd = mul_capped(mul_capped(mul_capped(mul_capped(d->B, d->Hkv), d->T), slots_in_memory(d)), d->d);
   if (q > kMaxElems || kd > kMaxElems) return MODA_ERR_INVALID_ARG;
   return MODA_OK;
 }
@@ -50,7 +54,8 @@ moda::Problem problem_of(const moda_desc* d) {
   p.H = d->H;
   p.Hkv = d->Hkv;
   p.T = d->T;
-  p.S = d->S;
+  p.S = d->S > 0 ? static_cast<int>(slots_in_memory(d)) : 0;  // memory stride (no depth when S = 0)
+  p.S_read = d->S;
   p.d = d->d;
   p.G = d->H / d->Hkv;
   p.scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->d));
@@ -202,7 +207,7 @@ moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* 
   if (cap < desc->T) return MODA_ERR_INVALID_ARG;
   // TMA row coordinates are 32-bit
   if (static_cast<int64_t>(desc->B) * desc->Hkv * cap >= (int64_t(1) << 31) ||
-      static_cast<int64_t>(desc->B) * desc->Hkv * desc->S >= (int64_t(1) << 31))
+      static_cast<int64_t>(desc->B) * desc->Hkv * slots_in_memory(desc) >= (int64_t(1) << 31))
     return MODA_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !o) return MODA_ERR_INVALID_ARG;
   if (desc->S > 0 && (!kd || !vd)) return MODA_ERR_INVALID_ARG;
@@ -233,7 +238,8 @@ moda_status moda_depth_store_kv(const moda_desc* desc, int32_t slot, const void*
   moda_status st = check_desc(desc);
   if (st != MODA_OK) return st;
   if (desc->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
-  if (desc->S < 1 || slot < 0 || slot >= desc->S) return MODA_ERR_INVALID_ARG;
+  const int64_t n_slots = slots_in_memory(desc);
+  if (n_slots < 1 || slot < 0 || slot >= n_slots) return MODA_ERR_INVALID_ARG;
   if (!k || !v || !kd || !vd) return MODA_ERR_INVALID_ARG;
   for (const void* p : {k, v, static_cast<const void*>(kd), static_cast<const void*>(vd)})
     if (!aligned16(p)) return MODA_ERR_INVALID_ARG;
@@ -241,7 +247,7 @@ moda_status moda_depth_store_kv(const moda_desc* desc, int32_t slot, const void*
   a.B = desc->B;
   a.Hkv = desc->Hkv;
   a.T = desc->T;
-  a.S = desc->S;
+  a.S = static_cast<int>(n_slots);
   a.d = desc->d;
   a.slot = slot;
   a.k = k;
@@ -259,7 +265,8 @@ moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d
   moda_status st = check_desc(desc);
   if (st != MODA_OK) return st;
   if (desc->dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
-  if (desc->S < 1 || slot < 0 || slot >= desc->S) return MODA_ERR_INVALID_ARG;
+  const int64_t n_slots = slots_in_memory(desc);
+  if (n_slots < 1 || slot < 0 || slot >= n_slots) return MODA_ERR_INVALID_ARG;
   if (d_model < 8 || d_model % 8 != 0) return MODA_ERR_INVALID_ARG;  // 16-byte row strides
   if ((desc->Hkv * desc->d) % 64 != 0) return MODA_ERR_UNSUPPORTED;
   if (desc->B > 65535 || (desc->T + 127) / 128 > 65535) return MODA_ERR_UNSUPPORTED;  // grid limits
@@ -271,7 +278,7 @@ moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d
   a.B = desc->B;
   a.Hkv = desc->Hkv;
   a.T = desc->T;
-  a.S = desc->S;
+  a.S = static_cast<int>(n_slots);
   a.d = desc->d;
   a.slot = slot;
   a.Dm = d_model;

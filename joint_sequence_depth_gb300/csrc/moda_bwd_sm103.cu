@@ -41,6 +41,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 struct BwdTcParams {
   int B, H, Hkv, T, S, G;
+  int S_read;  // slots read per position; dkd/dvd of slots S_read .. S-1 are written as zero
   float scale, scale_log2;
   const __nv_bfloat16 *q, *k, *v, *kd, *vd, *dout;
   const float* lse;
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 
   const int64_t slab = pid * p.S * D;
   auto load_slot = [&](int i, uint4& kv, uint4& vv) {
-    const bool sv = i < p.S;
+    const bool sv = i < p.S_read;
     kv = sv ? __ldg(reinterpret_cast<const uint4*>(p.kd + slab + static_cast<int64_t>(i) * D) + cc)
             : make_uint4(0, 0, 0, 0);
     vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
@@ -110,11 +111,11 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 #pragma unroll
     for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
   }
-  for (int i0 = 0; i0 < p.S; i0 += SPW) {
+  for (int i0 = 0; i0 < p.S_read; i0 += SPW) {
     const int i = i0 + j;
-    const bool sv = i < p.S;
+    const bool sv = i < p.S_read;
     const uint4 kv = kn, vv = vn;
-    if (i0 + SPW < p.S) load_slot(i + SPW, kn, vn);
+    if (i0 + SPW < p.S_read) load_slot(i + SPW, kn, vn);
     float s[HG], dp[HG];
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {
@@ -182,6 +183,11 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
       reinterpret_cast<uint4*>(p.dkd + slab + static_cast<int64_t>(i) * D)[cc] = ok;
       reinterpret_cast<uint4*>(p.dvd + slab + static_cast<int64_t>(i) * D)[cc] = ov;
     }
+  }
+  // slots in memory that are not read have zero gradient
+  for (int i = p.S_read + j; i < p.S; i += SPW) {
+    reinterpret_cast<uint4*>(p.dkd + slab + static_cast<int64_t>(i) * D)[cc] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(p.dvd + slab + static_cast<int64_t>(i) * D)[cc] = make_uint4(0, 0, 0, 0);
   }
   // dq depth share: reduce over the SPW slot groups, lanes of group 0 write float32
 #pragma unroll
@@ -1480,6 +1486,7 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.Hkv = pr.Hkv;
   p.T = pr.T;
   p.S = pr.S;
+  p.S_read = pr.S_read;
   p.G = pr.G;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale_log2;

@@ -18,7 +18,10 @@ constexpr int kStatusConfig = 3;   // a kernel refused its launch configuration 
 constexpr int kStatusTimeout = 4;  // a bounded wait ran out (MODA_ERR_TIMEOUT)
 
 struct Problem {
-  int B, H, Hkv, T, S, d, G;
+  int B, H, Hkv, T;
+  int S;       // depth slots per position in kd/vd memory (0: no depth memory)
+  int S_read;  // slots 0 .. S_read-1 of each position are read (S_read <= S; S_read = 0 iff S = 0)
+  int d, G;
   float scale;       // score scale (1/sqrt(d) by default)
   float scale_log2;  // scale * log2(e)
 };

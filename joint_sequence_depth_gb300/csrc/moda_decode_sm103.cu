@@ -54,6 +54,7 @@ struct DecCfg {
 
 struct DecParams {
   int B, H, Hkv, T, S, G;
+  int S_read;  // depth slots read (of the S in memory per (b, g))
   int n_seq;   // sequence splits (the depth split, when S > 0, is index n_seq)
   int chunk;   // sequence keys per split, a multiple of kDecKeys
   int64_t cap; // positions allocated per (b, g) in the sequence cache
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const bool depth = split == p.n_seq;
   const int k0 = depth ? 0 : split * p.chunk;
-  const int k1 = depth ? p.S : min(p.T, k0 + p.chunk);
+  const int k1 = depth ? p.S_read : min(p.T, k0 + p.chunk);
   const int n_keys = max(0, k1 - k0);
   const int n_sub = (n_keys + kDecKeys - 1) / kDecKeys;
   const CUtensorMap* mk = depth ? &tmKd : &tmK;
@@ -376,6 +377,7 @@ cudaError_t launch_dec(const DecodeArgs& a, const DecodeSplit& sp, cudaStream_t 
   p.Hkv = pr.Hkv;
   p.T = pr.T;
   p.S = pr.S;
+  p.S_read = pr.S_read;
   p.G = pr.G;
   p.n_seq = sp.n_seq;
   p.chunk = sp.chunk;

@@ -95,6 +95,7 @@ struct FwdCfg {
 
 struct FwdTcParams {
   int B, H, Hkv, T, S, G, P;
+  int S_read;   // slots read per position (the rest of the S in memory get P = 0)
   int n_pb;     // position blocks (of 2P positions) per (b, kv head)
   int n_units;  // B * Hkv * n_pb
   int n_cta;    // persistent CTAs
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int lo, hi;  // visible columns [lo, hi) of this row in this key tile
         if (depth) {
           const int k0 = j * BN;
-          if (wp_hi * p.S + p.S <= k0 || wp_lo * p.S >= k0 + BN) {
+          if (wp_hi * p.S + p.S_read <= k0 || wp_lo * p.S >= k0 + BN) {
             // no position of this warp has keys in this depth tile: P = 0
             if constexpr (C::SPLIT) {
               tc_fence_before();
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           lo = valid ? pl * p.S - k0 : BN;
-          hi = valid ? lo + p.S : BN;
+          hi = valid ? lo + p.S_read : BN;
         } else {
           const int kb = (j - p.n_d) * BN;
           lo = 0;
@@ -925,6 +926,7 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.Hkv = pr.Hkv;
   p.T = pr.T;
   p.S = pr.S;
+  p.S_read = pr.S_read;
   p.G = pr.G;
   p.P = BM / pr.G;
   p.n_pb = (pr.T + 2 * p.P - 1) / (2 * p.P);

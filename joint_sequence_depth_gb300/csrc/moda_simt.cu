@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const FwdArgs a) 
     const int64_t slab = (bg * p.T + t) * p.S * D + lane * N;
     const T* kd = static_cast<const T*>(a.kd) + slab;
     const T* vd = static_cast<const T*>(a.vd) + slab;
-    for (int i = 0; i < p.S; ++i) {
+    for (int i = 0; i < p.S_read; ++i) {
       load_frag(kd + static_cast<int64_t>(i) * D, kf);
       const float s2 = warp_sum(dot(qf, kf));
       load_frag(vd + static_cast<int64_t>(i) * D, vf);
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(const BwdArgs 
     const int64_t slab = (bg * p.T + t) * p.S * D + lane * N;
     const T* kd = static_cast<const T*>(a.kd) + slab;
     const T* vd = static_cast<const T*>(a.vd) + slab;
-    for (int i = 0; i < p.S; ++i) {
+    for (int i = 0; i < p.S_read; ++i) {
       load_frag(kd + static_cast<int64_t>(i) * D, kf);
       load_frag(vd + static_cast<int64_t>(i) * D, vf);
       const float pj = exp2f(warp_sum(dot(qf, kf)) - lse2);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_depth_simt_kernel(const BwdAr
   const int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
   const int64_t slab = (bg * p.T + t) * p.S * D + lane * N;
   float kf[N], vf[N], qf[N], df[N], dk[N], dv[N];
-  for (int i = 0; i < p.S; ++i) {
+  for (int i = 0; i < p.S_read; ++i) {
     load_frag(static_cast<const T*>(a.kd) + slab + static_cast<int64_t>(i) * D, kf);
     load_frag(static_cast<const T*>(a.vd) + slab + static_cast<int64_t>(i) * D, vf);
 #pragma unroll
@@ -270,6 +270,13 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_depth_simt_kernel(const BwdAr
     for (int c = 0; c < N; ++c) dk[c] *= p.scale;
     store_frag(static_cast<T*>(a.dkd) + slab + static_cast<int64_t>(i) * D, dk);
     store_frag(static_cast<T*>(a.dvd) + slab + static_cast<int64_t>(i) * D, dv);
+  }
+  // slots in memory that are not read have zero gradient
+#pragma unroll
+  for (int c = 0; c < N; ++c) dk[c] = 0.f;
+  for (int i = p.S_read; i < p.S; ++i) {
+    store_frag(static_cast<T*>(a.dkd) + slab + static_cast<int64_t>(i) * D, dk);
+    store_frag(static_cast<T*>(a.dvd) + slab + static_cast<int64_t>(i) * D, dk);
   }
 }
 
