@@ -83,10 +83,11 @@ def bytes_moved(shape):
     q = B * H * T * d * e
     kv = 2 * B * Hkv * T * d * e
     dkv = 2 * B * Hkv * T * S * d * e
+    dkv_mem = 2 * B * Hkv * T * shape.S_mem * d * e  # dkd/dvd cover every slot in memory
     lse = B * H * T * 4
-    fwd = q + kv + dkv + q + lse  # read q, k, v, kd, vd; write o, lse
-    bwd = (q + kv + dkv + q + q + lse) + (q + kv + dkv)  # read q,k,v,kd,vd,o,dout,lse; write dq..dvd
-    return {"fwd": fwd, "bwd": bwd, "inputs": q + kv + dkv + q, "outputs": q + lse + q + kv + dkv}
+    fwd = q + kv + dkv + q + lse  # read q, k, v, kd, vd (the S slots read); write o, lse
+    bwd = (q + kv + dkv + q + q + lse) + (q + kv + dkv_mem)  # read q,k,v,kd,vd,o,dout,lse; write dq..dvd
+    return {"fwd": fwd, "bwd": bwd, "inputs": q + kv + dkv_mem + q, "outputs": q + lse + q + kv + dkv_mem}
 
 
 def load_peaks():
@@ -192,7 +193,7 @@ def oracle_sample(shape, T_sample):
 
     from joint_sequence_depth_gb300.inputs import make_inputs, scaled
 
-    sub = scaled(shape, B=1, H=shape.G, Hkv=1, T=T_sample)
+    sub = scaled(shape, B=1, H=shape.G, Hkv=1, T=T_sample, slot_capacity=0)  # the S slots read
     x = make_inputs(sub, seed=101, device="cpu", with_dout=True)
     host = [x[n].view(torch.int16).numpy().view(np.uint16) if x[n].dtype == torch.bfloat16 else x[n].numpy()
             for n in ("q", "k", "v", "kd", "vd", "dout")]
@@ -281,10 +282,14 @@ def run_reference(args, shape):
 
 
 def workload_config(shape):
-    return {"workload": f"{shape.name}: B={shape.B} H={shape.H} Hkv={shape.Hkv} T={shape.T} d={shape.d} "
-                        f"S={shape.S} {shape.dtype_name}, causal, forward+backward",
-            "global_batch": shape.B, "seq_len": shape.T, "depth_slots": shape.S,
-            "l2": "inputs larger than L2 (no flush)"}
+    ring = f" read of {shape.S_mem} in memory (bounded slot buffer)" if shape.slot_capacity else ""
+    cfg = {"workload": f"{shape.name}: B={shape.B} H={shape.H} Hkv={shape.Hkv} T={shape.T} d={shape.d} "
+                       f"S={shape.S}{ring} {shape.dtype_name}, causal, forward+backward",
+           "global_batch": shape.B, "seq_len": shape.T, "depth_slots": shape.S,
+           "l2": "inputs larger than L2 (no flush)"}
+    if shape.slot_capacity:
+        cfg["slot_capacity"] = shape.slot_capacity
+    return cfg
 
 
 DECODE_METRIC = "MoDA decode step GB/s and fraction of the HBM roofline, 1\u00d7GB300"
@@ -660,13 +665,15 @@ def main():
     lse = torch.empty(base.B, base.H, base.T, dtype=torch.float32, device=dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(kd),
              torch.empty_like(vd))
-    desc = binding.make_desc(base.B, base.H, base.Hkv, base.T, base.S, base.d, base.dtype)
+    desc = binding.make_desc(base.B, base.H, base.Hkv, base.T, base.S, base.d, base.dtype,
+                             slot_capacity=base.slot_capacity)
+    slots = base.S if base.slot_capacity else None  # a ring: read the first S of S_mem slots
     ws = torch.empty(binding.moda_bwd_workspace_bytes(desc), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        binding.moda_fwd(q, k, v, kd, vd, o, lse)
-        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws)
+        binding.moda_fwd(q, k, v, kd, vd, o, lse, slots=slots)
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, slots=slots)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -685,9 +692,9 @@ def main():
     launches0 = binding.moda_launch_count()
     for i in range(K):
         ev[i][0].record(stream)
-        binding.moda_fwd(q, k, v, kd, vd, o, lse)
+        binding.moda_fwd(q, k, v, kd, vd, o, lse, slots=slots)
         ev[i][1].record(stream)
-        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:10])
+        binding.moda_bwd(q, k, v, kd, vd, o, lse, dout, grads, ws, events=ev[i][2:10], slots=slots)
     torch.cuda.synchronize()
     launches = binding.moda_launch_count() - launches0
     if world > 1:
@@ -742,9 +749,9 @@ def main():
             if i >= 2:
                 stream.wait_event(ev_d2h[i - 2])  # set i%2 outputs already copied out
             o_, l_, *g_ = dout_
-            binding.moda_fwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_)
+            binding.moda_fwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_, slots=slots)
             binding.moda_bwd(din["q"], din["k"], din["v"], din["kd"], din["vd"], o_, l_, din["dout"], tuple(g_),
-                             ws if i % 2 == 0 else ws2)
+                             ws if i % 2 == 0 else ws2, slots=slots)
             ev_comp[i].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_comp[i])

@@ -28,6 +28,13 @@ class Shape:
     S: int
     dtype: torch.dtype
     backward: bool = False
+    # bounded slot buffer: slots per position in kd/vd memory (0: exactly S); the first S
+    # are read, the rest stand for slots a ring has not filled yet
+    slot_capacity: int = 0
+
+    @property
+    def S_mem(self) -> int:
+        return self.slot_capacity if self.slot_capacity > 0 else self.S
 
     @property
     def G(self) -> int:
@@ -47,6 +54,9 @@ WORKLOADS = {
     "bf16_train": Shape("bf16_train", 8, 16, 4, 4096, 64, 32, torch.bfloat16, backward=True),
     # a quarter of the training batch: the size kernel profiles are captured on
     "bf16_train_quarter": Shape("bf16_train_quarter", 2, 16, 4, 4096, 64, 32, torch.bfloat16, backward=True),
+    # the training step while a 32-slot ring is half full: 16 slots read of 32 in memory
+    "bf16_train_ring_half": Shape("bf16_train_ring_half", 8, 16, 4, 4096, 64, 16, torch.bfloat16, backward=True,
+                                  slot_capacity=32),
 }
 
 # seed of each workload (its index in the list above, from 1)
@@ -70,8 +80,8 @@ def make_inputs(shape: Shape, seed: int, device="cpu", with_dout: bool | None = 
         "q": (B, H, T, d),
         "k": (B, Hkv, T, d),
         "v": (B, Hkv, T, d),
-        "kd": (B, Hkv, T, S, d),
-        "vd": (B, Hkv, T, S, d),
+        "kd": (B, Hkv, T, shape.S_mem, d),
+        "vd": (B, Hkv, T, shape.S_mem, d),
     }
     if with_dout:
         dims["dout"] = (B, H, T, d)
