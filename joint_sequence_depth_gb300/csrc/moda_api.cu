@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "moda.h"
 #include "moda_common.cuh"
@@ -14,6 +15,20 @@ namespace {
 std::atomic<int64_t> g_launches{0};
 }
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void* tensor_map_encoder() {
+  static void* fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = ptr;
+  });
+  return fn;
+}
 }  // namespace moda
 
 namespace {

@@ -1443,16 +1443,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
 
 // ============================================================================ host
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
 // bf16 [planes][T][D] as the 3-D tensor (D, T, planes), box 64 x rows x depth, 128-byte
@@ -1467,14 +1458,6 @@ bool make_map(CUtensorMap* map, const void* base, int D, int T, int planes, int 
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes, int& done) {
-  if (done >= bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done = bytes;
-  return e;
 }
 
 template <int D>
@@ -1544,10 +1527,10 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     const int pq2 = K2N / pr.G;
     if (!make_map(&tq2, a.q, D, pr.T, planes_q, pq2, pr.G) || !make_map(&to2, a.dout, D, pr.T, planes_q, pq2, pr.G))
       return cudaErrorInvalidValue;
-    static int smem_dkdv = 0, smem_dq = 0;
-    e = set_smem(moda_bwd_dkdv64_kernel, Dkv64Cfg::SMEM, smem_dkdv);
+    static std::atomic<uint64_t> smem_dkdv{0}, smem_dq{0};
+    e = ensure_dynamic_smem(moda_bwd_dkdv64_kernel, Dkv64Cfg::SMEM, smem_dkdv);
     if (e != cudaSuccess) return e;
-    e = set_smem(moda_bwd_dq64_kernel, Dq64Cfg::SMEM, smem_dq);
+    e = ensure_dynamic_smem(moda_bwd_dq64_kernel, Dq64Cfg::SMEM, smem_dq);
     if (e != cudaSuccess) return e;
     mark_event(a, 4, s);
     moda_bwd_dkdv64_kernel<<<grid_kv, Dkv64Cfg::THREADS, Dkv64Cfg::SMEM, s>>>(tk128, tv128, tq2, to2, p);
@@ -1560,10 +1543,10 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     // each tile's columns, one CTA per SM.
     using KC = DkvCfg<D, 2, 2>;
     using QC = DqCfg<D, 2, 2>;
-    static int smem_dkdv = 0, smem_dq = 0;
-    e = set_smem(moda_bwd_dkdv_kernel<D, 2, 2>, KC::SMEM, smem_dkdv);
+    static std::atomic<uint64_t> smem_dkdv{0}, smem_dq{0};
+    e = ensure_dynamic_smem(moda_bwd_dkdv_kernel<D, 2, 2>, KC::SMEM, smem_dkdv);
     if (e != cudaSuccess) return e;
-    e = set_smem(moda_bwd_dq_kernel<D, 2, 2>, QC::SMEM, smem_dq);
+    e = ensure_dynamic_smem(moda_bwd_dq_kernel<D, 2, 2>, QC::SMEM, smem_dq);
     if (e != cudaSuccess) return e;
     mark_event(a, 4, s);
     moda_bwd_dkdv_kernel<D, 2, 2><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);

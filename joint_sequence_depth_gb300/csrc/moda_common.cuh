@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace moda {
 
 // log2(e): the slides' Algorithm 1 uses 2^(S-m); folding log2(e) into the score
@@ -71,6 +73,27 @@ struct DepthWriteArgs {
   const void *k, *v, *x, *wk, *wv;
   void *kd, *vd;
 };
+
+// cuTensorMapEncodeTiled from the driver (looked up once, thread-safe); null when the
+// driver does not provide it.
+void* tensor_map_encoder();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device: the attribute belongs to the kernel's instance on each device, so a process that
+// drives several GPUs sets it on each.  `done` is the call site's per-device bit mask
+// (devices 0..63; a higher ordinal sets the attribute on every call).  Concurrent callers
+// may both set it, which is harmless.
+template <typename K>
+cudaError_t ensure_dynamic_smem(K kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Records a.events[k] on `s` when the caller asked for it (profiling only).
 inline void mark_event(const BwdArgs& a, int k, cudaStream_t s) {

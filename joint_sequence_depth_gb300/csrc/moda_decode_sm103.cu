@@ -318,16 +318,7 @@ __global__ void __launch_bounds__(128) moda_decode_merge_kernel(const DecMergePa
 
 // ---------------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 dec_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
 // bf16 rows [rows][D] as the 2-D tensor (D, rows), box 64 x kDecKeys, 128-byte swizzle.
@@ -348,14 +339,6 @@ int dec_sms() {
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 1;
   return std::max(n, 1);
-}
-
-template <typename K>
-cudaError_t dec_set_smem(K kernel, int bytes, int& done) {
-  if (done >= bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done = bytes;
-  return e;
 }
 
 template <int D, int HG>
@@ -387,8 +370,8 @@ cudaError_t launch_dec(const DecodeArgs& a, const DecodeSplit& sp, cudaStream_t 
   p.part = a.part;
   p.status = a.status;
   using C = DecCfg<D>;
-  static int done = 0;
-  cudaError_t e = dec_set_smem(moda_decode_kernel<D, HG>, C::SMEM, done);
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = ensure_dynamic_smem(moda_decode_kernel<D, HG>, C::SMEM, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(sp.n_split), static_cast<unsigned>(groups));
   moda_decode_kernel<D, HG><<<grid, DecWarps<HG>::THREADS, C::SMEM, s>>>(tk, tv, tkd, tvd, p);

@@ -228,16 +228,7 @@ __global__ void __launch_bounds__(128, 2)
 
 // ---------------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
 bool dw_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
@@ -306,12 +297,9 @@ cudaError_t launch_depth_project_sm103(const DepthWriteArgs& a, cudaStream_t s) 
   p.d = a.d;
   p.n_total = n_total;
   p.status = a.status;
-  static int done = 0;
-  if (done < P_SMEM) {
-    cudaError_t e = cudaFuncSetAttribute(moda_depth_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    if (e != cudaSuccess) return e;
-    done = P_SMEM;
-  }
+  static std::atomic<uint64_t> done{0};
+  cudaError_t e = ensure_dynamic_smem(moda_depth_project_kernel, P_SMEM, done);
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((n_total + PN - 1) / PN), static_cast<unsigned>((a.T + PM - 1) / PM),
                   static_cast<unsigned>(a.B));
   moda_depth_project_kernel<<<grid, 128, P_SMEM, s>>>(tx, twk, twv, tkd, tvd, p);

@@ -856,17 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
 
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
@@ -950,12 +940,9 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
     tkd = tk;  // never read
     tvd = tv;
   }
-  static int attr_set = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moda_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = 1;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  cudaError_t e = ensure_dynamic_smem(moda_fwd_tc_kernel<D>, C::SMEM, attr_set);
+  if (e != cudaSuccess) return e;
   moda_fwd_tc_kernel<D><<<p.n_cta, kThreads, C::SMEM, s>>>(tq, tk, tv, tkd, tvd, p);
   count_launches(1);
   return cudaGetLastError();

@@ -48,10 +48,10 @@ def test_status_strings_and_version(lib):
 
 
 def desc(**kw):
-    base = dict(B=1, H=4, Hkv=2, T=16, S=3, d=64, dtype=1, scale=0.0)
+    base = dict(B=1, H=4, Hkv=2, T=16, S=3, d=64, dtype=1, scale=0.0, slot_capacity=0)
     base.update(kw)
     return binding.moda_desc(base["B"], base["H"], base["Hkv"], base["T"], base["S"], base["d"], base["dtype"],
-                             base["scale"])
+                             base["scale"], base["slot_capacity"])
 
 
 FAKE = 1 << 20  # aligned fake device address: validation must fail before any use
@@ -65,6 +65,7 @@ def fwd(lib, d, ptrs=None):
 @pytest.mark.parametrize("kw,status", [
     (dict(H=3, Hkv=2), 1), (dict(T=0), 1), (dict(B=0), 1), (dict(S=-1), 1), (dict(Hkv=0), 1),
     (dict(d=96), 2), (dict(d=256), 2), (dict(dtype=7), 2), (dict(scale=float("nan")), 1),
+    (dict(slot_capacity=-1), 1), (dict(S=4, slot_capacity=3), 1),
 ])
 def test_forward_rejects_bad_desc(lib, kw, status):
     assert fwd(lib, desc(**kw)) == status
@@ -99,3 +100,46 @@ def test_backward_workspace_contract(lib):
     assert lib.moda_bwd(ctypes.byref(d), *ptrs, None, ctypes.c_size_t(need), None) == 5
     # workspace not 256-byte aligned
     assert lib.moda_bwd(ctypes.byref(d), *ptrs, ctypes.c_void_p(FAKE + 16), ctypes.c_size_t(need), None) == 1
+
+
+def test_depth_writes_reject_bad_arguments(lib):
+    """Slot out of range (of the slots in memory), fp32, null or misaligned pointers,
+    d_model not a multiple of 8: all refused before any launch."""
+    f = ctypes.c_void_p(FAKE)
+    store = lambda d, slot, ptrs=None: lib.moda_depth_store_kv(ctypes.byref(d), slot, *(ptrs or [f] * 4), None)  # noqa: E731
+    assert store(desc(S=3), -1) == 1
+    assert store(desc(S=3), 3) == 1
+    assert store(desc(S=3, slot_capacity=8), 8) == 1
+    assert store(desc(S=0), 0) == 1
+    assert store(desc(S=3, dtype=0), 0) == 2
+    for i in range(4):
+        bad = [f] * 4
+        bad[i] = None
+        assert store(desc(), 0, bad) == 1
+        bad[i] = ctypes.c_void_p(FAKE + 4)
+        assert store(desc(), 0, bad) == 1
+    project = lambda d, slot, dm, ptrs=None: lib.moda_depth_project_kv(  # noqa: E731
+        ctypes.byref(d), slot, dm, *(ptrs or [f] * 5), None)
+    assert project(desc(S=3), 3, 64) == 1
+    assert project(desc(S=3), 0, 12) == 1
+    assert project(desc(S=3), 0, 0) == 1
+    assert project(desc(S=3, dtype=0), 0, 64) == 2
+    for i in range(5):
+        bad = [f] * 5
+        bad[i] = ctypes.c_void_p(FAKE + 8)
+        assert project(desc(), 0, 64, bad) == 1
+
+
+def test_decode_rejects_bad_arguments(lib):
+    """Cache capacity below T, fp32, null pointers: refused before any launch."""
+    f = ctypes.c_void_p(FAKE)
+    dec = lambda d, cap, ptrs=None: lib.moda_decode(  # noqa: E731
+        ctypes.byref(d), ctypes.c_int64(cap), *(ptrs or [f] * 6), None, f, ctypes.c_size_t(1 << 20), None)
+    assert dec(desc(T=16), 15) == 1
+    assert dec(desc(dtype=0), 0) == 2
+    bad = [f] * 6  # q, k_cache, v_cache, kd, vd, o
+    bad[0] = None
+    assert dec(desc(), 0, bad) == 1
+    bad = [f] * 6
+    bad[3] = None  # depth keys missing while S > 0
+    assert dec(desc(S=3), 0, bad) == 1
