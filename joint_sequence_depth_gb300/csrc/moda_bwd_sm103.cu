@@ -828,19 +828,21 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
 // ============================================================================ dK / dV, d = 64
 // CTA: 128 keys [kb, kb+128) of (b, g).  Query tiles of 128 rows, head-major inside the
 // tile (row r -> head g*G + r/P2, position p0 + r%P2, P2 = floor(128/G)), so the S^T and
-// dP^T products have N = 128.  One CTA per SM, 320 threads.
+// dP^T products have N = 128.  One CTA per SM, 352 threads.
 // TMEM (512 columns): S^T [0,128), dP^T [128,256), P^T [256,320) and dS^T [320,384)
 // (bf16 pairs), dV [384,448), dK [448,512).  The gradient warps release S^T/dP^T as soon
 // as they have read them (s_free), so S^T and dP^T of tile i+1 are computed while P^T and
 // dS^T of tile i are formed; dV, dK of tile i follow (p_full), and their commit (q_empty)
 // frees both the Q/dO stage and P^T, dS^T.
-// Warps: 0 loads, 1 MMA issuer, 2..9 gradient warps: warpgroup w forms query columns
-// [64w, 64w+64) of every tile; thread = key = TMEM lane.
+// Warps: 0 loads, 1 issues S^T and dP^T, 10 issues dV and dK, 2..9 gradient warps:
+// warpgroup w forms query columns [64w, 64w+64) of every tile; thread = key = TMEM lane.
+// Two issuing threads, so that one waiting on a barrier (Q/dO loads and S^T released;
+// P^T, dS^T written) does not leave the tensor pipe's short queue empty.
 constexpr int K2N = 128;
 
 struct Dkv64Cfg {
   static constexpr int D = 64;
-  static constexpr int THREADS = 64 + 256;
+  static constexpr int THREADS = 64 + 256 + 32;
   static constexpr int KV_BYTES = KBM * D * 2;    // the CTA's K (or V) tile
   static constexpr int QT_BYTES = K2N * D * 2;    // one 128-row Q (or dO) tile
   static constexpr int NSTAGE = 4;
@@ -850,7 +852,7 @@ struct Dkv64Cfg {
   static constexpr int OFF_Q = 2 * KV_BYTES;      // stage s: Q at + s*STAGE, dO at + QT_BYTES
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][128] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * K2N * 8;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, (spare), drain, last_done
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, drain_g, drain, last_done
   static constexpr int NBAR = 1 + 2 * NSTAGE + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
@@ -887,6 +889,7 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
   uint64_t* s_full = q_empty + C::NSTAGE;
   uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;
+  uint64_t* drain_g = p_full + 1;
   uint64_t* drain = p_full + 2;
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -904,6 +907,7 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
     mbar_init(s_free, 8);  // one arrival per gradient warp
     mbar_init(p_full, 8);
     mbar_init(drain, 1);
+    mbar_init(drain_g, 1);
     mbar_init(last_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -978,59 +982,71 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
         mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S^T, dP^T issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(KBM, K2N, false);
-      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
       const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
       const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-      const uint64_t qt_desc_k = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);          // K-major Q/dO tiles
-      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, K2N * 128, 1024);  // MN-major Q/dO tiles
+      const uint64_t qt_desc_k = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);  // K-major Q/dO tiles
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      for (int i = 0; ok && i <= n_q; ++i) {
-        if (i < n_q) {
-          // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, once tile i is loaded and the gradient
-          // warps have read S^T/dP^T of tile i-1
-          const int st = i % C::NSTAGE;
-          ok = mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag) &&
-               (i == 0 || mbar_wait(s_free, (i - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t q_desc = sdesc_add(qt_desc_k, st * C::STAGE_BYTES);
-          const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
+      for (int i = 0; ok && i < n_q; ++i) {
+        // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T, once tile i is loaded and the gradient
+        // warps have read S^T/dP^T of tile i-1
+        const int st = i % C::NSTAGE;
+        ok = mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag) &&
+             (i == 0 || mbar_wait(s_free, (i - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t q_desc = sdesc_add(qt_desc_k, st * C::STAGE_BYTES);
+        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + C::TM_S, sdesc_add(k_desc, kk * 32), sdesc_add(q_desc, kk * 32), IDESC_S, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_S, sdesc_add(k_desc, kk * 32), sdesc_add(q_desc, kk * 32), IDESC_S, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + C::TM_DP, sdesc_add(v_desc, kk * 32), sdesc_add(o_desc, kk * 32), IDESC_S, kk > 0);
-          mma_commit(s_full);
-        }
-        if (i > 0) {
-          // dV += P^T(j) dO_j, dK += dS^T(j) Q_j for j = i-1
-          const int j = i - 1, st = j % C::NSTAGE;
-          ok = mbar_wait(p_full, j & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
-          const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < K2N / 16; ++kk)
-            mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < K2N / 16; ++kk)
-            mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DS + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&q_empty[st]);  // also tells the gradient warps that P^T(j), dS^T(j) are read
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_DP, sdesc_add(v_desc, kk * 32), sdesc_add(o_desc, kk * 32), IDESC_S, kk > 0);
+        mma_commit(s_full);
       }
-      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
         volatile int never = 0;
         mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp == 10) {
+    // ---------------------------------------------------------------- dV, dK issuer
+    // dV, dK of tile j follow p_full(j), which the gradient warps signal only after reading
+    // S^T(j), dP^T(j): those MMAs have completed, so this thread's commit after dV, dK of
+    // tile j is the last use of the Q/dO stage and of P^T, dS^T.
+    if (lane == 0) {
+      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
+      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, K2N * 128, 1024);  // MN-major Q/dO tiles
+      bool ok = true;
+      for (int j = 0; ok && j < n_q; ++j) {
+        // dV += P^T(j) dO_j, dK += dS^T(j) Q_j
+        const int st = j % C::NSTAGE;
+        ok = mbar_wait(p_full, j & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
+        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < K2N / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < K2N / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DS + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&q_empty[st]);  // also tells the gradient warps that P^T(j), dS^T(j) are read
+      }
+      if (ok) mma_commit(last_done);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain_g);
+        volatile int never = 0;
+        mbar_wait(drain_g, 0, &never);
       }
     }
   } else {
@@ -1153,16 +1169,19 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
 // ============================================================================ dQ, d = 64
 // CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G, head
 // g*G + r%G), P = floor(128/G) positions.  Key tiles of 128, so S and dP have N = 128.
-// One CTA per SM, 320 threads.  TMEM (512 columns): S [0,128), dP [128,256) (released as
+// One CTA per SM, 352 threads.  TMEM (512 columns): S [0,128), dP [128,256) (released as
 // soon as the gradient warps have read them, so S and dP of tile j+1 are computed while
 // dS of tile j is formed), dS[2] [256,320), [320,384) (bf16 pairs, double-buffered),
-// dQ [384,448).  Warps: 0 loads K_j, V_j; 1 MMA issuer; 2..9 gradient warps (warpgroup w
-// forms key columns [64w, 64w+64) of every tile; warpgroup 0 also stages Q and dO).
+// dQ [384,448).  Warps: 0 loads K_j, V_j; 1 issues S and dP; 10 issues dQ; 2..9 gradient
+// warps (warpgroup w forms key columns [64w, 64w+64) of every tile; warpgroup 0 also
+// stages Q and dO).  Two issuing threads, because a thread that waits on a barrier lets
+// the tensor pipe's short queue run dry: the S/dP thread waits for K/V and for the
+// gradient warps to release S, the dQ thread for dS, each while the other's MMAs run.
 constexpr int Q2N = 128;
 
 struct Dq64Cfg {
   static constexpr int D = 64;
-  static constexpr int THREADS = 64 + 256;
+  static constexpr int THREADS = 64 + 256 + 32;
   static constexpr int KV_BYTES = Q2N * D * 2;  // one K (or V) tile; a ring slot holds both
   static constexpr int NSLOT = 3;
   static constexpr int Q_BYTES = QBM * D * 2;
@@ -1170,7 +1189,7 @@ struct Dq64Cfg {
   static constexpr int OFF_DO = Q_BYTES;
   static constexpr int OFF_KV = 2 * Q_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, (2 spare), drain, last_done
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, (spare), drain, last_done
   static constexpr int NBAR = 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
@@ -1207,6 +1226,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   uint64_t* s_full = q_full + 1;
   uint64_t* s_free = s_full + 1;
   uint64_t* ds_full = s_free + 1;
+  uint64_t* drain_dq = ds_full + 1;
   uint64_t* drain = ds_full + 3;
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -1222,6 +1242,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     mbar_init(s_free, 8);  // one arrival per gradient warp
     mbar_init(ds_full, 8);
     mbar_init(drain, 1);
+    mbar_init(drain_dq, 1);
     mbar_init(last_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -1262,55 +1283,66 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S, dP issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, Q2N, false);
-      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t do_desc = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);           // K-major
-      const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, Q2N * 128, 1024);   // MN-major
+      const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);  // K-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          // S(j) = Q K_j^T and dP(j) = dO V_j^T, once K_j, V_j are loaded and the gradient
-          // warps have read S/dP of tile j-1
-          const int slot = j % C::NSLOT;
-          ok = mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag) &&
-               (j == 0 || mbar_wait(s_free, (j - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
-          const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        // S(j) = Q K_j^T and dP(j) = dO V_j^T, once K_j, V_j are loaded and the gradient
+        // warps have read S/dP of tile j-1
+        const int slot = j % C::NSLOT;
+        ok = mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag) &&
+             (j == 0 || mbar_wait(s_free, (j - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
+        const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + C::TM_S, sdesc_add(q_desc, kk * 32), sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_S, sdesc_add(q_desc, kk * 32), sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + C::TM_DP, sdesc_add(do_desc, kk * 32), sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
-          mma_commit(s_full);
-        }
-        if (j > 0) {
-          // dQ += dS(jj) K_jj for jj = j-1
-          const int jj = j - 1, slot = jj % C::NSLOT;
-          ok = mbar_wait(ds_full, jj & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
-          const uint32_t ds = C::TM_DS + (jj & 1) * 64;
-#pragma unroll
-          for (int kk = 0; kk < Q2N / 16; ++kk)
-            mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
-                        (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&kv_empty[slot]);  // K_jj, V_jj and dS(jj) no longer read
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_DP, sdesc_add(do_desc, kk * 32), sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
+        mma_commit(s_full);
       }
-      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
         volatile int never = 0;
         mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp == 10) {
+    // ---------------------------------------------------------------- dQ issuer
+    // dQ(j) is issued after ds_full(j), which the gradient warps signal only after reading
+    // S(j), dP(j): those MMAs have completed, so this thread's commit after dQ(j) is the
+    // last use of K_j, V_j and frees their slot.
+    if (lane == 0) {
+      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
+      const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, Q2N * 128, 1024);  // MN-major
+      bool ok = true;
+      for (int jj = 0; ok && jj < n_kv; ++jj) {
+        const int slot = jj % C::NSLOT;
+        ok = mbar_wait(ds_full, jj & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
+        const uint32_t ds = C::TM_DS + (jj & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < Q2N / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&kv_empty[slot]);  // K_jj, V_jj and dS(jj) no longer read
+      }
+      if (ok) mma_commit(last_done);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain_dq);
+        volatile int never = 0;
+        mbar_wait(drain_dq, 0, &never);
       }
     }
   } else {
