@@ -1072,6 +1072,10 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
       const int p0 = (qt0 + i) * P2;
       const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
       const int dk = key - p0;
+      // P^T and dS^T of both 32-column halves first, in registers; only then wait until the
+      // dV/dK products of tile i-1 have read the single P^T, dS^T buffer (their commit
+      // completes tile i-1's phase of q_empty), so that wait overlaps this tile's arithmetic
+      uint32_t pp[32], pd[32];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int c0 = wg * 64 + hf * 32;  // first query column of this group
@@ -1096,7 +1100,6 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
             for (int c = 0; c < 32; ++c) e[c] = (dk > (c0 + c) % P2) ? 0.f : e[c];
           }
         }
-        uint32_t pp[16], pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float4 dl = sl[K2N / 4 + ((c0 + c) >> 2)];  // Delta of rows c0+c .. c0+c+3
@@ -1105,21 +1108,19 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
                    e[c + 1], d0, d1);
           fsubmul2(__uint_as_float(dpv[hf * 32 + c + 2]), __uint_as_float(dpv[hf * 32 + c + 3]), dl.z, dl.w,
                    e[c + 2], e[c + 3], d2, d3);
-          pp[c >> 1] = pack_bf16(e[c], e[c + 1]);
-          pp[(c >> 1) + 1] = pack_bf16(e[c + 2], e[c + 3]);
-          pd[c >> 1] = pack_bf16(d0, d1);
-          pd[(c >> 1) + 1] = pack_bf16(d2, d3);
+          pp[hf * 16 + (c >> 1)] = pack_bf16(e[c], e[c + 1]);
+          pp[hf * 16 + (c >> 1) + 1] = pack_bf16(e[c + 2], e[c + 3]);
+          pd[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
+          pd[hf * 16 + (c >> 1) + 1] = pack_bf16(d2, d3);
         }
-        // P^T and dS^T of tile i-1 must have been read by its dV/dK products first
-        // (their commit completes tile i-1's phase of q_empty)
-        if (hf == 0 && i > 0) {
-          ok = warp_wait(&q_empty[(i - 1) % C::NSTAGE], ((i - 1) / C::NSTAGE) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        tmem_st16_nowait(tmem + lane_base + C::TM_P + wg * 32 + hf * 16, pp);
-        tmem_st16_nowait(tmem + lane_base + C::TM_DS + wg * 32 + hf * 16, pd);
       }
+      if (i > 0) {
+        ok = warp_wait(&q_empty[(i - 1) % C::NSTAGE], ((i - 1) / C::NSTAGE) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32_nowait(tmem + lane_base + C::TM_P + wg * 32, pp);
+      tmem_st32_nowait(tmem + lane_base + C::TM_DS + wg * 32, pd);
       if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
