@@ -140,17 +140,9 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
         dp[hh] += __shfl_xor_sync(0xffffffffu, dp[hh], off);
       }
     }
-    float kf[8], vf[8];
-    {
-      const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        kf[2 * c] = bf16_lo(kw[c]);
-        kf[2 * c + 1] = bf16_hi(kw[c]);
-        vf[2 * c] = bf16_lo(vw[c]);
-        vf[2 * c + 1] = bf16_hi(vw[c]);
-      }
-    }
+    // P and dS enter the gradient products rounded to bf16, as in the tensor-core kernels,
+    // so every product is a mixed-precision FMA on the stored bf16 pairs (no widening)
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
     float gk[8], gv[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) gk[c] = gv[c] = 0.f;
@@ -158,17 +150,15 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
     for (int hh = 0; hh < HG; ++hh) {
       const float pr = sv ? ex2(fmaf(s[hh], p.scale_log2, -lse2[hh])) : 0.f;
       const float ds = pr * (dp[hh] - dl[hh]);
+      const uint32_t pd = pack_bf16(pr, ds);  // P in the low half, dS in the high half
       const uint32_t qw[4] = {qv[hh].x, qv[hh].y, qv[hh].z, qv[hh].w};
       const uint32_t ow[4] = {dv4[hh].x, dv4[hh].y, dv4[hh].z, dv4[hh].w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        gk[2 * c] = fmaf(ds, bf16_lo(qw[c]), gk[2 * c]);
-        gk[2 * c + 1] = fmaf(ds, bf16_hi(qw[c]), gk[2 * c + 1]);
-        gv[2 * c] = fmaf(pr, bf16_lo(ow[c]), gv[2 * c]);
-        gv[2 * c + 1] = fmaf(pr, bf16_hi(ow[c]), gv[2 * c + 1]);
+        axpy2_bf16_hi(pd, qw[c], gk[2 * c], gk[2 * c + 1]);
+        axpy2_bf16(pd, ow[c], gv[2 * c], gv[2 * c + 1]);
+        axpy2_bf16_hi(pd, kw[c], dq[hh][2 * c], dq[hh][2 * c + 1]);
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) dq[hh][c] = fmaf(ds, kf[c], dq[hh][c]);
     }
     if (sv) {
       uint4 ok, ov;
