@@ -55,15 +55,21 @@ struct BwdTcParams {
 // ============================================================================ depth
 // One warp per position (b, g, t).  Lane = (slot sub-index j, 16-byte column chunk cc):
 // a warp step covers SPW = 32 / (d/8) consecutive slots, each slot row read with one
-// coalesced 16-byte load per lane.  The G heads of the position (HG >= G) stay in
+// coalesced 16-byte copy per lane, staged by cp.async through a per-warp ring of
+// kDepthStages steps in shared memory (three steps in flight, no registers held; a lane
+// only reads back the chunks it copied itself, so the group wait alone orders them).  The G heads of the position (HG >= G) stay in
 // registers (q, dO packed bf16), so each depth element is read from HBM once and used
 // for all G heads.  The warp also forms the row statistics of its G rows,
 // {-lse * log2(e), Delta = dO . O}, and stores them for the dK/dV and dQ kernels.
+constexpr int kDepthStages = 4;
+
 template <int D, int HG>
 __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p) {
   constexpr int CH = D / 8;
   constexpr int SPW = 32 / CH;
-  const int lane = threadIdx.x & 31;
+  constexpr int NB = kDepthStages;
+  __shared__ __align__(16) uint4 stage[8][NB][2][32];  // [warp][step % NB][k, v][lane]
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t pid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (pid >= static_cast<int64_t>(p.B) * p.Hkv * p.T) return;
   const int t = static_cast<int>(pid % p.T);
@@ -72,15 +78,20 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
   const int j = lane / CH, cc = lane % CH;
 
   const int64_t slab = pid * p.S * D;
-  auto load_slot = [&](int i, uint4& kv, uint4& vv) {
+  const int n_steps = (p.S_read + SPW - 1) / SPW;
+  // copy step `st` (slots st*SPW + j) into ring entry st % NB; slots past S_read read as zero
+  auto issue = [&](int st) {
+    const int i = st * SPW + j;
     const bool sv = i < p.S_read;
-    kv = sv ? __ldg(reinterpret_cast<const uint4*>(p.kd + slab + static_cast<int64_t>(i) * D) + cc)
-            : make_uint4(0, 0, 0, 0);
-    vv = sv ? __ldg(reinterpret_cast<const uint4*>(p.vd + slab + static_cast<int64_t>(i) * D) + cc)
-            : make_uint4(0, 0, 0, 0);
+    const int64_t off = sv ? slab + static_cast<int64_t>(i) * D + cc * 8 : 0;
+    cp_async_16_zfill(smem_u32(&stage[wib][st % NB][0][lane]), p.kd + off, sv);
+    cp_async_16_zfill(smem_u32(&stage[wib][st % NB][1][lane]), p.vd + off, sv);
   };
-  uint4 kn, vn;  // next step's slot rows, loaded one step ahead (issued before the row loads)
-  load_slot(j, kn, vn);
+#pragma unroll
+  for (int st = 0; st < NB - 1; ++st) {  // issued before the row loads
+    if (st < n_steps) issue(st);
+    cp_async_commit();
+  }
   uint4 qv[HG], dv4[HG], ov[HG];
   float lse2[HG], dl[HG], dq[HG][8];
   int64_t rows[HG];
@@ -111,11 +122,13 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 #pragma unroll
     for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
   }
-  for (int i0 = 0; i0 < p.S_read; i0 += SPW) {
-    const int i = i0 + j;
+  for (int st = 0; st < n_steps; ++st) {
+    const int i = st * SPW + j;
     const bool sv = i < p.S_read;
-    const uint4 kv = kn, vv = vn;
-    if (i0 + SPW < p.S_read) load_slot(i + SPW, kn, vn);
+    if (st + NB - 1 < n_steps) issue(st + NB - 1);
+    cp_async_commit();
+    cp_async_wait<NB - 1>();  // this thread's copies of step st have landed
+    const uint4 kv = stage[wib][st % NB][0][lane], vv = stage[wib][st % NB][1][lane];
     float s[HG], dp[HG];
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {

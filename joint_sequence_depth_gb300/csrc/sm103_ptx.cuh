@@ -414,6 +414,20 @@ __device__ __forceinline__ void fsubmul2(float a0, float a1, float b0, float b1,
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// 16-byte asynchronous global -> shared copy through L2 only; when `valid` is false nothing
+// is read and the 16 bytes are zeroed.  Completion is tracked by commit groups.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst_smem, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's most recent commit groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 8-byte asynchronous global -> shared copy (see cp_async_4).
 __device__ __forceinline__ void cp_async_8(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(src))
