@@ -56,12 +56,12 @@ struct BwdTcParams {
 // One warp per position (b, g, t).  Lane = (slot sub-index j, 16-byte column chunk cc):
 // a warp step covers SPW = 32 / (d/8) consecutive slots, each slot row read with one
 // coalesced 16-byte copy per lane, staged by cp.async through a per-warp ring of
-// kDepthStages steps in shared memory (three steps in flight, no registers held; a lane
+// kDepthStages steps in shared memory (seven steps in flight, no registers held; a lane
 // only reads back the chunks it copied itself, so the group wait alone orders them).  The G heads of the position (HG >= G) stay in
 // registers (q, dO packed bf16), so each depth element is read from HBM once and used
 // for all G heads.  The warp also forms the row statistics of its G rows,
 // {-lse * log2(e), Delta = dO . O}, and stores them for the dK/dV and dQ kernels.
-constexpr int kDepthStages = 4;
+constexpr int kDepthStages = 8;
 
 template <int D, int HG>
 __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p) {
