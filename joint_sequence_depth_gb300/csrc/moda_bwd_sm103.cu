@@ -1176,9 +1176,10 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
 // One CTA per SM, 352 threads.  TMEM (512 columns): S [0,128), dP [128,256) (released as
 // soon as the gradient warps have read them, so S and dP of tile j+1 are computed while
 // dS of tile j is formed), dS[2] [256,320), [320,384) (bf16 pairs, double-buffered),
-// dQ [384,448).  Warps: 0 loads K_j, V_j; 1 issues S and dP; 10 issues dQ; 2..9 gradient
-// warps (warpgroup w forms key columns [64w, 64w+64) of every tile; warpgroup 0 also
-// stages Q and dO).  Two issuing threads, because a thread that waits on a barrier lets
+// dQ [384,448), Q [448,480) and dO [480,512) (bf16 pairs: the A operands of S and dP, so
+// those products read only K and V from shared memory).  Warps: 0 loads K_j, V_j; 1
+// issues S and dP; 10 issues dQ; 2..9 gradient warps (warpgroup w forms key columns
+// [64w, 64w+64) of every tile; warpgroup 0 also writes Q and dO into TMEM).  Two issuing threads, because a thread that waits on a barrier lets
 // the tensor pipe's short queue run dry: the S/dP thread waits for K/V and for the
 // gradient warps to release S, the dQ thread for dS, each while the other's MMAs run.
 constexpr int Q2N = 128;
@@ -1188,16 +1189,14 @@ struct Dq64Cfg {
   static constexpr int THREADS = 64 + 256 + 32;
   static constexpr int KV_BYTES = Q2N * D * 2;  // one K (or V) tile; a ring slot holds both
   static constexpr int NSLOT = 3;
-  static constexpr int Q_BYTES = QBM * D * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = Q_BYTES;
-  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int OFF_KV = 0;  // Q and dO live in TMEM, not here
   static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
   // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, (spare), drain, last_done
   static constexpr int NBAR = 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DS = 256, TM_DQ = 384;
+  // Q and dO of the CTA's rows stay in TMEM (A operands of S and dP, bf16 pairs)
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DS = 256, TM_DQ = 384, TM_Q = 448, TM_DO = 480;
   static constexpr uint32_t TM_COLS = 512;
 };
 
@@ -1290,8 +1289,6 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     // ---------------------------------------------------------------- S, dP issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, Q2N, false);
-      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t do_desc = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);  // K-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -1306,10 +1303,10 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
         const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_S, sdesc_add(q_desc, kk * 32), sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
+          mma_bf16_ts(tmem + C::TM_S, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_DP, sdesc_add(do_desc, kk * 32), sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
+          mma_bf16_ts(tmem + C::TM_DP, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
         mma_commit(s_full);
       }
       if (!ok) {
@@ -1359,15 +1356,28 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     const int h = g * p.G + r % p.G;
     const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
     if (wg == 0) {
+      // row r of Q and dO into TMEM lane r (the A operands of S and dP): column c holds
+      // elements 2c, 2c+1, i.e. the row's 32-bit words as stored
       const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
       const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
+      uint32_t qw[32], ow[32];
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {
-        const uint32_t off = sw128_offset(r, ch);
-        st_shared_v4(sbase + C::OFF_Q + off, valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0));
-        st_shared_v4(sbase + C::OFF_DO + off, valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0));
+        const uint4 a = valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0);
+        const uint4 o = valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0);
+        qw[4 * ch] = a.x;
+        qw[4 * ch + 1] = a.y;
+        qw[4 * ch + 2] = a.z;
+        qw[4 * ch + 3] = a.w;
+        ow[4 * ch] = o.x;
+        ow[4 * ch + 1] = o.y;
+        ow[4 * ch + 2] = o.z;
+        ow[4 * ch + 3] = o.w;
       }
-      fence_proxy_async_smem();
+      tmem_st32_nowait(tmem + lane_base + C::TM_Q, qw);
+      tmem_st32_nowait(tmem + lane_base + C::TM_DO, ow);
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(q_full);
     }
     const float2 stt = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
