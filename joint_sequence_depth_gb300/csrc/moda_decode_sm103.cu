@@ -44,7 +44,9 @@ struct DecWarps {
 template <int D>
 struct DecCfg {
   static constexpr int TILE_BYTES = kDecKeys * D * 2;  // one K (or V) sub-tile, bf16
-  static constexpr int NSTAGE = D == 128 ? 2 : 3;
+  // Few stages, many resident CTAs: one 64 KB stage at d = 128 (two CTAs per SM), two
+  // 32 KB stages at d = 64 (three per SM); the other CTAs on the SM hide each one's loads.
+  static constexpr int NSTAGE = D == 128 ? 1 : 2;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K then V
   static constexpr int OFF_Q = NSTAGE * STAGE_BYTES;   // float q [kDecMaxG][D], scale*log2(e) folded in
   static constexpr int OFF_RED = OFF_Q + kDecMaxG * D * 4;  // [4 warps][kDecMaxG][D + 2] float
