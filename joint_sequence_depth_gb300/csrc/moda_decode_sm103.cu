@@ -44,13 +44,16 @@ struct DecWarps {
 template <int D>
 struct DecCfg {
   static constexpr int TILE_BYTES = kDecKeys * D * 2;  // one K (or V) sub-tile, bf16
-  // Few stages, many resident CTAs: one 64 KB stage at d = 128 (two CTAs per SM), two
-  // 32 KB stages at d = 64 (three per SM); the other CTAs on the SM hide each one's loads.
+  // Few stages, many resident CTAs: one 64 KB stage at d = 128, two 32 KB stages at d = 64
+  // (three CTAs per SM either way); the other CTAs on the SM hide each one's loads.
   static constexpr int NSTAGE = D == 128 ? 1 : 2;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K then V
   static constexpr int OFF_Q = NSTAGE * STAGE_BYTES;   // float q [kDecMaxG][D], scale*log2(e) folded in
-  static constexpr int OFF_RED = OFF_Q + kDecMaxG * D * 4;  // [4 warps][kDecMaxG][D + 2] float
-  static constexpr int OFF_BAR = OFF_RED + 4 * kDecMaxG * (D + 2) * 4;
+  // [4 warps][kDecMaxG][D + 2] float, used only after the last K/V stage has been read and
+  // no copy is in flight: it shares the stage memory
+  static constexpr int OFF_RED = 0;
+  static_assert(4 * kDecMaxG * (D + 2) * 4 <= NSTAGE * STAGE_BYTES, "reduction area");
+  static constexpr int OFF_BAR = OFF_Q + kDecMaxG * D * 4;
   static constexpr int SMEM = OFF_BAR + NSTAGE * 8 + 16;
 };
 
