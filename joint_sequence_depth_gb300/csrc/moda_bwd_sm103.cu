@@ -230,18 +230,19 @@ template <int D, int NBUF, int NWG>
 struct DqCfg {
   static constexpr int THREADS = 64 + 128 * NWG;
   static constexpr int KV_BYTES = QBN * D * 2;  // one K (or V) tile; a ring slot holds both
-  static constexpr int NSLOT = NBUF == 2 ? 3 : 4;
-  static constexpr int Q_BYTES = QBM * D * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = Q_BYTES;
-  static constexpr int OFF_KV = 2 * Q_BYTES;
+  static constexpr int NSLOT = 4;
+  static constexpr int OFF_KV = 0;  // Q and dO live in TMEM
   static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
   // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[NBUF], ds_full[NBUF], drain, last_done
   static constexpr int NBAR = 2 * NSLOT + 3 + 2 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DQ = 128 * NBUF;
-  static constexpr uint32_t TM_COLS = (TM_DQ + D) <= 256 ? 256 : 512;
+  // Q and dO of the CTA's rows (bf16 pairs, D/2 columns each) are the A operands of S, dP
+  static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DQ = 128 * NBUF, TM_Q = TM_DQ + D, TM_DO = TM_Q + D / 2;
+  static constexpr uint32_t TM_COLS = (TM_DO + D / 2) <= 256 ? 256 : 512;
+  static_assert(TM_DO + D / 2 <= 512, "TMEM columns");
+  // a CTA that takes all 512 columns must be alone on its SM: shared memory keeps a second out
+  static_assert(TM_COLS < 512 || SMEM > 116 * 1024, "one CTA per SM");
 };
 
 template <int D, int NBUF, int NWG>
@@ -336,8 +337,6 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, QBN, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       // descriptors built once; each MMA only advances the start address
-      const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t do_desc = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
       const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, QBN * 128, 1024);    // MN-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
@@ -349,15 +348,13 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
         const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (QBM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_S + bf * QBN, sdesc_add(q_desc, aoff), sdesc_add(k_desc, boff), IDESC_S, kk > 0);
+          mma_bf16_ts(tmem + C::TM_S + bf * QBN, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, boff), IDESC_S, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (QBM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TM_DP + bf * QBN, sdesc_add(do_desc, aoff), sdesc_add(v_desc, boff), IDESC_S, kk > 0);
+          mma_bf16_ts(tmem + C::TM_DP + bf * QBN, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, boff), IDESC_S, kk > 0);
         }
         mma_commit(&s_full[bf]);
         return true;
@@ -398,15 +395,28 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
     const int h = g * p.G + r % p.G;
     const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
     if (wg == 0) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
-      const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
+      // row r of Q and dO into TMEM lane r, 32 columns (64 elements) at a time: column c
+      // holds elements 2c, 2c+1, the row's 32-bit words as stored
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        const uint4* src = reinterpret_cast<const uint4*>((part ? p.dout : p.q) + row * D);
+        const uint32_t dst = tmem + lane_base + (part ? C::TM_DO : C::TM_Q);
 #pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch) {
-        const uint32_t off = (ch >> 3) * (QBM * 128) + sw128_offset(r, ch & 7);
-        st_shared_v4(sbase + C::OFF_Q + off, valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0));
-        st_shared_v4(sbase + C::OFF_DO + off, valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0));
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t w[32];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 a = valid ? __ldg(src + c0 / 4 + ch) : make_uint4(0, 0, 0, 0);
+            w[4 * ch] = a.x;
+            w[4 * ch + 1] = a.y;
+            w[4 * ch + 2] = a.z;
+            w[4 * ch + 3] = a.w;
+          }
+          tmem_st32_nowait(dst + c0, w);
+        }
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(q_full);
     }
     const float2 st = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
