@@ -7,7 +7,8 @@
 //
 // The step is bound by HBM: each cached K/V row is read once for the G query heads of
 // its kv head.  The keys are split (flash-decoding): CTA (split, b*Hkv + g) streams its
-// key range in sub-tiles of 128 keys through a TMA ring (128-byte swizzle); the extra
+// key range in sub-tiles of 128 keys through one K and one V slot (TMA, 128-byte swizzle,
+// K of the next sub-tile loading while P V of this one runs); the extra
 // last split of each (b, g) takes the S depth slots.  Per sub-tile, lane = key for the
 // scores (q in shared memory, read as broadcasts), then lane = d/32 output columns for
 // P V (P broadcast by shuffles).  Each warp keeps, per head, a running max,
@@ -44,17 +45,17 @@ struct DecWarps {
 template <int D>
 struct DecCfg {
   static constexpr int TILE_BYTES = kDecKeys * D * 2;  // one K (or V) sub-tile, bf16
-  // Few stages, many resident CTAs: one 64 KB stage at d = 128, two 32 KB stages at d = 64
-  // (three CTAs per SM either way); the other CTAs on the SM hide each one's loads.
-  static constexpr int NSTAGE = D == 128 ? 1 : 2;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K then V
-  static constexpr int OFF_Q = NSTAGE * STAGE_BYTES;   // float q [kDecMaxG][D], scale*log2(e) folded in
-  // [4 warps][kDecMaxG][D + 2] float, used only after the last K/V stage has been read and
-  // no copy is in flight: it shares the stage memory
+  // One K slot and one V slot, each with a barrier of its own, and many resident CTAs
+  // (three per SM at d = 128, six at d = 64): the other CTAs on the SM hide each one's
+  // loads, and K of the next sub-tile loads while this one's softmax and P V run.
+  static constexpr int OFF_K = 0, OFF_V = TILE_BYTES;
+  static constexpr int OFF_Q = 2 * TILE_BYTES;  // float q [kDecMaxG][D], scale*log2(e) folded in
+  // [4 warps][kDecMaxG][D + 2] float, used only after the last sub-tile has been read and
+  // no copy is in flight: it shares the K/V slots
   static constexpr int OFF_RED = 0;
-  static_assert(4 * kDecMaxG * (D + 2) * 4 <= NSTAGE * STAGE_BYTES, "reduction area");
-  static constexpr int OFF_BAR = OFF_Q + kDecMaxG * D * 4;
-  static constexpr int SMEM = OFF_BAR + NSTAGE * 8 + 16;
+  static_assert(4 * kDecMaxG * (D + 2) * 4 <= 2 * TILE_BYTES, "reduction area");
+  static constexpr int OFF_BAR = OFF_Q + kDecMaxG * D * 4;  // k_full, v_full
+  static constexpr int SMEM = OFF_BAR + 2 * 8 + 16;
 };
 
 struct DecParams {
@@ -121,13 +122,17 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   const CUtensorMap* mv = depth ? &tmVd : &tmV;
   const int row0 = depth ? bg * p.S : static_cast<int>(bg * p.cap) + k0;  // host checks the int range
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NSTAGE * 8);
+  // K of sub-tile s + 1 is loaded as soon as every warp has its scores for sub-tile s,
+  // while the softmax and P V of s still run; V of s + 1 once P V of s is done
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* v_full = k_full + 1;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 2 * 8);
   float* qs = reinterpret_cast<float*>(smem + C::OFF_Q);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NSTAGE; ++i) mbar_init(&full[i], 1);
+    mbar_init(k_full, 1);
+    mbar_init(v_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -139,20 +144,22 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     qs[i] = x;
   }
   __syncthreads();
-  auto issue = [&](int s) {
-    const int st = s % C::NSTAGE;
-    uint8_t* dst = smem + st * C::STAGE_BYTES;
-    mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+  // K (kind 0) or V (kind 1) of sub-tile s into its slot
+  auto issue = [&](int s, int kind) {
+    uint8_t* dst = smem + (kind ? C::OFF_V : C::OFF_K);
+    uint64_t* bar = kind ? v_full : k_full;
+    mbar_arrive_expect_tx(bar, C::TILE_BYTES);
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_2d(dst + h * (kDecKeys * 128), mk, &full[st], h * 64, row0 + s * kDecKeys);
-      tma_load_2d(dst + C::TILE_BYTES + h * (kDecKeys * 128), mv, &full[st], h * 64, row0 + s * kDecKeys);
-    }
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_2d(dst + h * (kDecKeys * 128), kind ? mv : mk, bar, h * 64, row0 + s * kDecKeys);
   };
   if (threadIdx.x == 0) {
     prefetch_tmap(mk);
     prefetch_tmap(mv);
-    for (int s = 0; s < min(n_sub, C::NSTAGE); ++s) issue(s);
+    if (n_sub > 0) {
+      issue(0, 0);
+      issue(0, 1);
+    }
   }
 
   float m[HS], l[HS], o[HS][CPL];
@@ -164,16 +171,15 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     for (int c = 0; c < CPL; ++c) o[hh][c] = 0.f;
   }
   const int r = kw * 32 + lane;  // this lane's key row within a sub-tile
-  int issued = min(n_sub, C::NSTAGE);
+  int issued_k = min(n_sub, 1), issued_v = issued_k;  // sub-tiles whose K / V loads are issued
   bool failed = false;
   for (int s = 0; s < n_sub; ++s) {
-    const int st = s % C::NSTAGE;
-    const bool ok = mbar_wait(&full[st], (s / C::NSTAGE) & 1, abort_flag);
-    if (__syncthreads_or(!ok)) {  // block-uniform
+    const uint32_t par = s & 1;
+    if (__syncthreads_or(!mbar_wait(k_full, par, abort_flag))) {  // block-uniform
       failed = true;
       break;
     }
-    const uint32_t kt = sbase + st * C::STAGE_BYTES, vt = kt + C::TILE_BYTES;
+    const uint32_t kt = sbase + C::OFF_K, vt = sbase + C::OFF_V;
     const int base_key = s * kDecKeys;
     // ---- scores of the G heads for key r (two partial sums per head)
     float a0[HS], a1[HS];
@@ -194,6 +200,10 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
         ffma2(q1.z, q1.w, k6f, k7f, a0[hh], a1[hh], a0[hh], a1[hh]);
       }
     }
+    // every warp has read K: load the next sub-tile's K
+    __syncthreads();
+    if (threadIdx.x == 0 && issued_k < n_sub) issue(issued_k, 0);
+    ++issued_k;
     const bool valid = base_key + r < n_keys;
     // ---- online softmax per head: warp-wide max, per-lane sums
     float pr[HS];
@@ -210,6 +220,10 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < CPL; ++c) o[hh][c] *= corr;
       m[hh] = m_new;
+    }
+    if (__syncthreads_or(!mbar_wait(v_full, par, abort_flag))) {
+      failed = true;
+      break;
     }
     // ---- P V over this warp's valid keys; lane owns columns [lane*CPL, lane*CPL + CPL)
     const int n_here = min(32, n_keys - base_key - kw * 32);  // warp-uniform
@@ -235,18 +249,18 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
         for (int c = 0; c < CPL; c += 2) ffma2(pj, pj, vf[c], vf[c + 1], o[hh][c], o[hh][c + 1], o[hh][c], o[hh][c + 1]);
       }
     }
-    // every warp is done with this stage: refill it
+    // every warp has read V: load the next sub-tile's V
     __syncthreads();
-    if (threadIdx.x == 0 && issued < n_sub) issue(issued);
-    ++issued;
+    if (threadIdx.x == 0 && issued_v < n_sub) issue(issued_v, 1);
+    ++issued_v;
   }
   if (failed) {
     if (threadIdx.x == 0) {
       record_status(p.status, kStatusTimeout);
       // let the copies still in flight land before the CTA exits
       volatile int never = 0;
-      for (int s = max(0, issued - C::NSTAGE); s < min(issued, n_sub); ++s)
-        mbar_wait(&full[s % C::NSTAGE], (s / C::NSTAGE) & 1, &never);
+      if (issued_k > 0 && issued_k <= n_sub) mbar_wait(k_full, (issued_k - 1) & 1, &never);
+      if (issued_v > 0 && issued_v <= n_sub) mbar_wait(v_full, (issued_v - 1) & 1, &never);
     }
     return;
   }
