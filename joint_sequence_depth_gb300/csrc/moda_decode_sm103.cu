@@ -54,7 +54,10 @@ struct DecCfg {
   // no copy is in flight: it shares the K/V slots
   static constexpr int OFF_RED = 0;
   static_assert(4 * kDecMaxG * (D + 2) * 4 <= 2 * TILE_BYTES, "reduction area");
-  static constexpr int OFF_BAR = OFF_Q + kDecMaxG * D * 4;  // k_full, v_full
+  // float p [4 warps][32 keys][kDecMaxG]: the probabilities of each warp's keys, read back
+  // as broadcasts in P V (one shared load per key instead of one shuffle per head)
+  static constexpr int OFF_P = OFF_Q + kDecMaxG * D * 4;
+  static constexpr int OFF_BAR = OFF_P + 4 * 32 * kDecMaxG * 4;  // k_full, v_full
   static constexpr int SMEM = OFF_BAR + 2 * 8 + 16;
 };
 
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   uint64_t* v_full = k_full + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 2 * 8);
   float* qs = reinterpret_cast<float*>(smem + C::OFF_Q);
+  float* pw = reinterpret_cast<float*>(smem + C::OFF_P) + kw * 32 * HS;  // this warp's [32][HS]
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   if (threadIdx.x == 0) {
@@ -225,6 +229,11 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
       failed = true;
       break;
     }
+    // this lane's probabilities for the warp's P V loop (the previous sub-tile's loop has
+    // read its values before the barriers above)
+#pragma unroll
+    for (int hh = 0; hh < HS; ++hh) pw[lane * HS + hh] = pr[hh];
+    __syncwarp();
     // ---- P V over this warp's valid keys; lane owns columns [lane*CPL, lane*CPL + CPL)
     const int n_here = min(32, n_keys - base_key - kw * 32);  // warp-uniform
     const int xc = (lane * CPL) >> 3, sub = ((lane * CPL) & 7) * 2;
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
       }
 #pragma unroll
       for (int hh = 0; hh < HS; ++hh) {
-        const float pj = __shfl_sync(0xffffffffu, pr[hh], j);
+        const float pj = pw[j * HS + hh];
 #pragma unroll
         for (int c = 0; c < CPL; c += 2) ffma2(pj, pj, vf[c], vf[c + 1], o[hh][c], o[hh][c + 1], o[hh][c], o[hh][c + 1]);
       }
