@@ -216,14 +216,15 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 // ============================================================================ dQ
 // CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G,
 // head g*G + r%G), P = floor(128/G) positions.  Keys in tiles of 64.
+// Used at d = 128 (d = 64 has a kernel of its own below).
 // Warps: 0 TMA (K_j and V_j in one transaction), 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient
 // warps (warp w owns TMEM lanes 32*(w%4) ..; with two warpgroups WG k handles key
-// columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also loads Q
-// and dO).  NBUF S/dP buffers: with 2 the tensor cores compute tile j+1 while tile j's
-// dS is formed; with 1 (d = 64) the TMEM footprint is 256 columns so two CTAs share an
-// SM and overlap each other instead.
-// TMEM: S[b] cols [64b, 64b+64), dP[b] [64(NBUF+b), ...), dQ [128 NBUF, 128 NBUF + d).
-// dS (bf16) is written over the first 32 columns of S[b].
+// columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also writes the
+// CTA's Q and dO rows into TMEM).  NBUF S/dP buffers: with 2 the tensor cores compute
+// tile j+1 while tile j's dS is formed.
+// TMEM: S[b] cols [64b, 64b+64), dP[b] [64(NBUF+b), ...), dQ [128 NBUF, 128 NBUF + d),
+// then Q and dO (bf16 pairs, d/2 columns each: the A operands of S and dP).  dS (bf16)
+// is written over the first 32 columns of S[b].
 constexpr int QBM = 128, QBN = 64;
 
 template <int D, int NBUF, int NWG>
@@ -1183,9 +1184,9 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
 // ============================================================================ dQ, d = 64
 // CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G, head
 // g*G + r%G), P = floor(128/G) positions.  Key tiles of 128, so S and dP have N = 128.
-// One CTA per SM, 352 threads.  TMEM (512 columns): S [0,128), dP [128,256) (released as
-// soon as the gradient warps have read them, so S and dP of tile j+1 are computed while
-// dS of tile j is formed), dS[2] [256,320), [320,384) (bf16 pairs, double-buffered),
+// One CTA per SM, 352 threads.  TMEM (512 columns): S [0,128), dP [128,256) (each
+// completed and released through barriers of its own: P is formed from S while dP is
+// still computed, and S and dP of tile j+1 are computed while dS of tile j is formed), dS[2] [256,320), [320,384) (bf16 pairs, double-buffered),
 // dQ [384,448), Q [448,480) and dO [480,512) (bf16 pairs: the A operands of S and dP, so
 // those products read only K and V from shared memory).  Warps: 0 loads K_j, V_j; 1
 // issues S and dP; 10 issues dQ; 2..9 gradient warps (warpgroup w forms key columns
@@ -1201,8 +1202,9 @@ struct Dq64Cfg {
   static constexpr int NSLOT = 3;
   static constexpr int OFF_KV = 0;  // Q and dO live in TMEM, not here
   static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, (spare), drain, last_done
-  static constexpr int NBAR = 2 * NSLOT + 8;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, (spare), drain, last_done,
+  // dp_full, dp_free
+  static constexpr int NBAR = 2 * NSLOT + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   // Q and dO of the CTA's rows stay in TMEM (A operands of S and dP, bf16 pairs)
@@ -1242,6 +1244,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   uint64_t* drain_dq = ds_full + 1;
   uint64_t* drain = ds_full + 3;
   uint64_t* last_done = drain + 1;
+  uint64_t* dp_full = last_done + 1;  // S and dP complete, and are released, separately
+  uint64_t* dp_free = dp_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -1253,6 +1257,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     mbar_init(q_full, 128);
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);  // one arrival per gradient warp
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 8);
     mbar_init(ds_full, 8);
     mbar_init(drain, 1);
     mbar_init(drain_dq, 1);
@@ -1302,8 +1308,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);  // K-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       for (int j = 0; ok && j < n_kv; ++j) {
-        // S(j) = Q K_j^T and dP(j) = dO V_j^T, once K_j, V_j are loaded and the gradient
-        // warps have read S/dP of tile j-1
+        // S(j) = Q K_j^T once K_j, V_j are loaded and the gradient warps have read S of
+        // tile j-1; dP(j) = dO V_j^T once they have read dP of tile j-1
         const int slot = j % C::NSLOT;
         ok = mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag) &&
              (j == 0 || mbar_wait(s_free, (j - 1) & 1, abort_flag));
@@ -1314,10 +1320,14 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ts(tmem + C::TM_S, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
+        mma_commit(s_full);
+        ok = j == 0 || mbar_wait(dp_free, (j - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16_ts(tmem + C::TM_DP, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
-        mma_commit(s_full);
+        mma_commit(dp_full);
       }
       if (!ok) {
         raise_abort(abort_flag, p.status);
@@ -1399,33 +1409,43 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       ok = warp_wait(s_full, j & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[64], dpv[64];
-      tmem_ld64x2(tmem + lane_base + C::TM_S + wg * 64, tmem + lane_base + C::TM_DP + wg * 64, s, dpv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      const uint32_t ds = C::TM_DS + (j & 1) * 64 + wg * 32;
+      // P from S first, while dP may still be computed; then dS = P (dP - Delta)
+      float e[64];
+      {
+        uint32_t s[64];
+        tmem_ld64(tmem + lane_base + C::TM_S + wg * 64, s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int lim = valid ? pos - (j * Q2N + wg * 64 + hf * 32) : -1;  // columns c <= lim are visible
-        float e[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          ffma2(__uint_as_float(s[hf * 32 + c]), __uint_as_float(s[hf * 32 + c + 1]), sl2, sl2, nlse2, nlse2, e[c],
-                e[c + 1]);
+        for (int c = 0; c < 64; c += 2) {
+          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
           e[c] = ex2(e[c]);
           e[c + 1] = ex2(e[c + 1]);
         }
-        if (lim < 31) {
+        const int lim = valid ? pos - (j * Q2N + wg * 64) : -1;  // columns c <= lim are visible
+        if (lim < 63) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+          for (int c = 0; c < 64; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
         }
+      }
+      ok = warp_wait(dp_full, j & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld64(tmem + lane_base + C::TM_DP + wg * 64, dpv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);
+      const uint32_t ds = C::TM_DS + (j & 1) * 64 + wg * 32;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float d0, d1;
-          fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dlt, dlt, e[c],
-                   e[c + 1], d0, d1);
+          fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dlt, dlt,
+                   e[hf * 32 + c], e[hf * 32 + c + 1], d0, d1);
           pk[c >> 1] = pack_bf16(d0, d1);
         }
         // dS buffer (j & 1) was last read by the dQ product of tile j-2 (its commit
