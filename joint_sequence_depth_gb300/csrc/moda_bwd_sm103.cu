@@ -541,8 +541,9 @@ struct DkvCfg {
   static constexpr int OFF_Q = 2 * KV_BYTES;     // stage s: Q at + s*STAGE, dO at + QT_BYTES
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][64] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * 2 * KBN * 4;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[NBUF], p_full[NBUF], drain, last_done
-  static constexpr int NBAR = 3 + 2 * NSTAGE + 2 * NBUF;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[NBUF], p_full[NBUF], drain, last_done,
+  // dp_full[NBUF] (S^T and dP^T of a buffer complete separately)
+  static constexpr int NBAR = 3 + 2 * NSTAGE + 3 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DV = 128 * NBUF, TM_DK = 128 * NBUF + D;
@@ -579,6 +580,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   uint64_t* p_full = s_full + NBUF;
   uint64_t* drain = p_full + NBUF;
   uint64_t* last_done = drain + 1;
+  uint64_t* dp_full = last_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const float4* stat = reinterpret_cast<const float4*>(smem + C::OFF_STAT);  // two rows per float4
@@ -591,6 +593,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
     }
     for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
+      mbar_init(&dp_full[i], 1);
       mbar_init(&p_full[i], 128 * NWG);
     }
     mbar_init(drain, 1);
@@ -694,13 +697,14 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
           const uint32_t boff = (kk >> 2) * (KBN * 128) + (kk & 3) * 32;
           mma_bf16_ss(tmem + C::TM_S + bf * KBN, sdesc_add(k_desc, aoff), sdesc_add(q_desc, boff), IDESC_S, kk > 0);
         }
+        mma_commit(&s_full[bf]);  // the gradient warps form P^T while dP^T is computed
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * (KBM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (KBN * 128) + (kk & 3) * 32;
           mma_bf16_ss(tmem + C::TM_DP + bf * KBN, sdesc_add(v_desc, aoff), sdesc_add(o_desc, boff), IDESC_S, kk > 0);
         }
-        mma_commit(&s_full[bf]);
+        mma_commit(&dp_full[bf]);
         return true;
       };
       auto issue_g = [&](int i) -> bool {
@@ -751,37 +755,49 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       const float4* sl = stat + st * (KBN / 2);
       const int p0 = (qt0 + i) * Pq;
       const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
-      uint32_t pp[NCOL / 2], pd[NCOL / 2];
+      // P^T of this warpgroup's columns from S^T first, while dP^T may still be computed
+      float e[NCOL];
 #pragma unroll
       for (int hf = 0; hf < NCOL / 32; ++hf) {
         const int c0 = wg * NCOL + hf * 32;
-        uint32_t s[32], dpv[32];
-        tmem_ld32x2(tmem + lane_base + C::TM_S + bf * KBN + c0, tmem + lane_base + C::TM_DP + bf * KBN + c0, s, dpv);
-        float e[32];
+        uint32_t s[32];
+        tmem_ld32(tmem + lane_base + C::TM_S + bf * KBN + c0, s);
+        float* ee = e + hf * 32;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const float4 rs = sl[(c0 + c) >> 1];  // rows c0+c, c0+c+1: {-lse2, Delta, -lse2, Delta}
-          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, rs.x, rs.z, e[c], e[c + 1]);
-          e[c] = ex2(e[c]);
-          e[c + 1] = ex2(e[c + 1]);
+          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, rs.x, rs.z, ee[c], ee[c + 1]);
+          ee[c] = ex2(ee[c]);
+          ee[c + 1] = ex2(ee[c + 1]);
         }
         if (diag) {
           // row r sits at position p0 + r % Pq (head-major tile); keys after it are masked
           const int dk = key - p0;
           if ((Pq & (Pq - 1)) == 0) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) e[c] = (dk > ((c0 + c) & (Pq - 1))) ? 0.f : e[c];
+            for (int c = 0; c < 32; ++c) ee[c] = (dk > ((c0 + c) & (Pq - 1))) ? 0.f : ee[c];
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) e[c] = (dk > (c0 + c) % Pq) ? 0.f : e[c];
+            for (int c = 0; c < 32; ++c) ee[c] = (dk > (c0 + c) % Pq) ? 0.f : ee[c];
           }
         }
+      }
+      ok = warp_wait(&dp_full[bf], (i / NBUF) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t pp[NCOL / 2], pd[NCOL / 2];
+#pragma unroll
+      for (int hf = 0; hf < NCOL / 32; ++hf) {
+        const int c0 = wg * NCOL + hf * 32;
+        uint32_t dpv[32];
+        tmem_ld32(tmem + lane_base + C::TM_DP + bf * KBN + c0, dpv);
+        const float* ee = e + hf * 32;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const float4 rs = sl[(c0 + c) >> 1];
           float d0, d1;
-          fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), rs.y, rs.w, e[c], e[c + 1], d0, d1);
-          pp[hf * 16 + (c >> 1)] = pack_bf16(e[c], e[c + 1]);
+          fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), rs.y, rs.w, ee[c], ee[c + 1], d0, d1);
+          pp[hf * 16 + (c >> 1)] = pack_bf16(ee[c], ee[c + 1]);
           pd[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
         }
       }
