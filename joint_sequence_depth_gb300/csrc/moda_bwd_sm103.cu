@@ -59,7 +59,10 @@ struct BwdTcParams {
 // kDepthStages steps in shared memory (seven steps in flight, no registers held; a lane
 // only reads back the chunks it copied itself, so the group wait alone orders them).  The G heads of the position (HG >= G) stay in
 // registers (q, dO packed bf16), so each depth element is read from HBM once and used
-// for all G heads.  The warp also forms the row statistics of its G rows,
+// for all G heads.  Each lane's partial dot products are summed over the slot's lanes by
+// shuffles; with four heads a reduce-scatter hands every lane one full sum, so each
+// head's P and dS are formed by two lanes and then gathered.  The warp also forms the row
+// statistics of its G rows,
 // {-lse * log2(e), Delta = dO . O}, and stores them for the dK/dV and dQ kernels.
 constexpr int kDepthStages = 8;
 
@@ -122,6 +125,22 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
 #pragma unroll
     for (int c = 0; c < 8; ++c) dq[hh][c] = 0.f;
   }
+  // Four heads: the CH lanes of a slot hold 8 partial sums each (the scores and dP of the
+  // four heads).  After plain butterfly steps down to groups of 8 lanes (d = 128), a
+  // reduce-scatter leaves lane cc with the full sum number cc % 8 (head (cc % 8)/2; score
+  // for even, dP for odd): at d = 64 7 shuffles instead of 24, at d = 128 15 instead of
+  // 32; each head's P and dS are formed by its two lanes only, then gathered
+  constexpr bool kScatter = CH >= 8 && HG == 4;
+  float my_lse2 = 0.f, my_dl = 0.f;  // statistics of head (cc % 8)/2
+  if constexpr (kScatter) {
+    const int hm = (cc & 7) >> 1;
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh)
+      if (hh == hm) {
+        my_lse2 = lse2[hh];
+        my_dl = dl[hh];
+      }
+  }
   for (int st = 0; st < n_steps; ++st) {
     const int i = st * SPW + j;
     const bool sv = i < p.S_read;
@@ -144,26 +163,63 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
       s[hh] = a;
       dp[hh] = c2;
     }
-    // full dot products: reduce over the CH lanes of this slot
-#pragma unroll
-    for (int off = CH / 2; off >= 1; off >>= 1) {
-#pragma unroll
-      for (int hh = 0; hh < HG; ++hh) {
-        s[hh] += __shfl_xor_sync(0xffffffffu, s[hh], off);
-        dp[hh] += __shfl_xor_sync(0xffffffffu, dp[hh], off);
-      }
-    }
     // P and dS enter the gradient products rounded to bf16, as in the tensor-core kernels,
     // so every product is a mixed-precision FMA on the stored bf16 pairs (no widening)
+    uint32_t pdv[HG];  // per head: P in the low half, dS in the high half
+    if constexpr (kScatter) {
+      float v[8];
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        v[2 * hh] = s[hh];
+        v[2 * hh + 1] = dp[hh];
+      }
+#pragma unroll
+      for (int off = CH / 2; off >= 8; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], off);
+      // reduce-scatter over 8 lanes: keep the half named by each low bit of cc
+      const bool b2 = (cc & 4) != 0, b1 = (cc & 2) != 0, b0 = (cc & 1) != 0;
+      float w4[4], w2[2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float send = b2 ? v[u] : v[u + 4];
+        w4[u] = (b2 ? v[u + 4] : v[u]) + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float send = b1 ? w4[u] : w4[u + 2];
+        w2[u] = (b1 ? w4[u + 2] : w4[u]) + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      const float mine = (b0 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b0 ? w2[0] : w2[1], 1);
+      const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+      const float sc = b0 ? other : mine, dpp = b0 ? mine : other;
+      const float pr = sv ? ex2(fmaf(sc, p.scale_log2, -my_lse2)) : 0.f;
+      const uint32_t pd = pack_bf16(pr, pr * (dpp - my_dl));
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) pdv[hh] = __shfl_sync(0xffffffffu, pd, (lane & ~(CH - 1)) | (2 * hh));
+    } else {
+      // full dot products: reduce over the CH lanes of this slot
+#pragma unroll
+      for (int off = CH / 2; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int hh = 0; hh < HG; ++hh) {
+          s[hh] += __shfl_xor_sync(0xffffffffu, s[hh], off);
+          dp[hh] += __shfl_xor_sync(0xffffffffu, dp[hh], off);
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < HG; ++hh) {
+        const float pr = sv ? ex2(fmaf(s[hh], p.scale_log2, -lse2[hh])) : 0.f;
+        pdv[hh] = pack_bf16(pr, pr * (dp[hh] - dl[hh]));
+      }
+    }
     const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
     float gk[8], gv[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) gk[c] = gv[c] = 0.f;
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {
-      const float pr = sv ? ex2(fmaf(s[hh], p.scale_log2, -lse2[hh])) : 0.f;
-      const float ds = pr * (dp[hh] - dl[hh]);
-      const uint32_t pd = pack_bf16(pr, ds);  // P in the low half, dS in the high half
+      const uint32_t pd = pdv[hh];
       const uint32_t qw[4] = {qv[hh].x, qv[hh].y, qv[hh].z, qv[hh].w};
       const uint32_t ow[4] = {dv4[hh].x, dv4[hh].y, dv4[hh].z, dv4[hh].w};
 #pragma unroll
