@@ -248,22 +248,58 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
     reinterpret_cast<uint4*>(p.dkd + slab + static_cast<int64_t>(i) * D)[cc] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(p.dvd + slab + static_cast<int64_t>(i) * D)[cc] = make_uint4(0, 0, 0, 0);
   }
-  // dq depth share: reduce over the SPW slot groups, lanes of group 0 write float32
-#pragma unroll
-  for (int off = CH; off < 32; off <<= 1) {
+  // dq depth share: sum over the SPW slot groups and write float32
+  if constexpr (kScatter) {
+    // reduce-scatter over the groups: group j ends with the full sums of heads
+    // j*(4/SPW) .. j*(4/SPW) + 4/SPW - 1, and writes them
+    constexpr int NV = HG * 8;
+    float val[NV];
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) dq[hh][c] += __shfl_xor_sync(0xffffffffu, dq[hh][c], off);
-  }
-  if (j == 0) {
+      for (int c = 0; c < 8; ++c) val[hh * 8 + c] = dq[hh][c];
+    int n = NV;
 #pragma unroll
-    for (int hh = 0; hh < HG; ++hh) {
+    for (int off = 16; off >= CH; off >>= 1) {
+      const bool bit = (lane & off) != 0;
+      n >>= 1;
+#pragma unroll
+      for (int u = 0; u < NV / 2; ++u) {
+        if (u < n) {
+          const float send = bit ? val[u] : val[u + n];
+          val[u] = (bit ? val[u + n] : val[u]) + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+    }
+    constexpr int NH = 4 / SPW;  // heads per group
+#pragma unroll
+    for (int u = 0; u < NH; ++u) {
+      const int hh = j * NH + u;
       if (hh < p.G) {
         const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + t;
         float4* dst = reinterpret_cast<float4*>(p.dq_accum + row * D + cc * 8);
-        dst[0] = make_float4(dq[hh][0] * p.scale, dq[hh][1] * p.scale, dq[hh][2] * p.scale, dq[hh][3] * p.scale);
-        dst[1] = make_float4(dq[hh][4] * p.scale, dq[hh][5] * p.scale, dq[hh][6] * p.scale, dq[hh][7] * p.scale);
+        const float* w = val + u * 8;
+        dst[0] = make_float4(w[0] * p.scale, w[1] * p.scale, w[2] * p.scale, w[3] * p.scale);
+        dst[1] = make_float4(w[4] * p.scale, w[5] * p.scale, w[6] * p.scale, w[7] * p.scale);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int off = CH; off < 32; off <<= 1) {
+#pragma unroll
+      for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) dq[hh][c] += __shfl_xor_sync(0xffffffffu, dq[hh][c], off);
+    }
+    if (j == 0) {
+#pragma unroll
+      for (int hh = 0; hh < HG; ++hh) {
+        if (hh < p.G) {
+          const int64_t row = (static_cast<int64_t>(b) * p.H + g * p.G + hh) * p.T + t;
+          float4* dst = reinterpret_cast<float4*>(p.dq_accum + row * D + cc * 8);
+          dst[0] = make_float4(dq[hh][0] * p.scale, dq[hh][1] * p.scale, dq[hh][2] * p.scale, dq[hh][3] * p.scale);
+          dst[1] = make_float4(dq[hh][4] * p.scale, dq[hh][5] * p.scale, dq[hh][6] * p.scale, dq[hh][7] * p.scale);
+        }
       }
     }
   }
