@@ -37,7 +37,7 @@
 //                 S[t] and O_t += P_t V (P_t read from TMEM), so the tensor core works on
 //                 one tile while the other tile's softmax runs.
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: thread r owns row r
-//               (TMEM lane r), S read in two halves of 64 keys; exp2 with a log2(e)-folded
+//               (TMEM lane r), S read whole (128 columns); exp2 with a log2(e)-folded
 //               scale; P rounded to bf16 into the TMEM columns of S; O rescaled only when the running max of a row that
 //               already holds probability mass grows by more than 2^8 (exact: the final
 //               division uses the same stale max); a warp none of whose positions a depth
@@ -654,13 +654,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi = (kb + BN - 1 > pfirst || !valid) ? (valid ? pos - kb + 1 : 0) : BN;
         }
         float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
-        if constexpr (C::SPLIT) {
-          // S read whole, then handed back to the MMA issuer for the next key tile
+        {
+          // S read whole (d = 64: then handed back to the MMA issuer for the next key tile;
+          // d = 128: P is written over it once every column is in registers)
           uint32_t s[BN];
           tmem_ld128(s_tmem, s);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[t]);
+          if constexpr (C::SPLIT) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[t]);
+          }
           if (lo > 0 || hi < BN) {
 #pragma unroll
             for (int c = 0; c < BN; ++c)
@@ -675,7 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
           }
           const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-          bool pv_waited = j == 0;  // P_t is free once the previous PV of this tile completed
+          // P_t is free once the previous PV of this tile completed (d = 128: S of this step,
+          // issued after that PV, is complete, so it has)
+          bool pv_waited = j == 0 || !C::SPLIT;
           const bool need = m_tile > m_run + kRescaleThreshold;  // includes the first keys of a row
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? fmaxf(m_run, m_tile) : m_run;
@@ -683,10 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float corr = (m_run == -INFINITY || !need) ? 1.f : ex2(m_run - m_new);
             if (__any_sync(0xffffffffu, corr != 1.f)) {
               // the previous PV of this tile must have landed in O before it is rescaled
-              ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-              pv_waited = true;
+              if (!pv_waited) {
+                ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                pv_waited = true;
+              }
 #pragma unroll 1
               for (int c = 0; c < D / 16; ++c) {
                 uint32_t o[16];
@@ -725,83 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           tmem_st64(p_tmem, pk);
-        } else {
-        // Two halves of 64 keys.  P of the first half is written (over S columns already
-        // read) before the second half is loaded; if the second half raises the running max
-        // of a row that holds mass past the threshold, the first half's P is rescaled in
-        // place together with O and l.
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t s[64];
-          tmem_ld64(s_tmem + half * 64, s);
-          const int lo_h = lo - half * 64, hi_h = hi - half * 64;
-          if (lo_h > 0 || hi_h < 64) {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c < lo_h || c >= hi_h) s[c] = __float_as_uint(-INFINITY);
-          }
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
-          }
-          const float m_h = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-          const bool need = m_h > m_run + kRescaleThreshold;  // includes the first keys of a row
-          if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? fmaxf(m_run, m_h) : m_run;
-            // a row that holds no mass yet (m_run = -inf) needs no rescale
-            const float corr = (m_run == -INFINITY || !need) ? 1.f : ex2(m_run - m_new);
-            if (__any_sync(0xffffffffu, corr != 1.f)) {
-              if (j > 0) {
-                // the previous PV of this tile has landed in O: S of this step, issued after
-                // it, is complete
-#pragma unroll 1
-                for (int c = 0; c < D / 16; ++c) {
-                  uint32_t o[16];
-                  tmem_ld16(o_tmem + c * 16, o);
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-                  tmem_st16(o_tmem + c * 16, o);
-                }
-              }
-              if (half == 1) {
-                uint32_t pw[32];
-                tmem_ld32(s_tmem, pw);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pw[i] = pack_bf16(bf16_lo(pw[i]) * corr, bf16_hi(pw[i]) * corr);
-                tmem_st32(s_tmem, pw);
-              }
-            }
-            l_run *= corr;
-            ls0 *= corr;
-            ls1 *= corr;
-            ls2 *= corr;
-            ls3 *= corr;
-            m_run = m_new;
-          }
-          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            float x0, x1, x2, x3;
-            ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
-            ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
-            x0 = ex2(x0);
-            x1 = ex2(x1);
-            x2 = ex2(x2);
-            x3 = ex2(x3);
-            if ((c & 4) == 0)
-              fadd2(ls0, ls1, x0, x1), fadd2(ls0, ls1, x2, x3);
-            else
-              fadd2(ls2, ls3, x0, x1), fadd2(ls2, ls3, x2, x3);
-            pk[c >> 1] = pack_bf16(x0, x1);
-            pk[(c >> 1) + 1] = pack_bf16(x2, x3);
-          }
-          tmem_st32(s_tmem + half * 32, pk);
-        }
         }
         if (!ok) break;
         l_run += (ls0 + ls1) + (ls2 + ls3);
