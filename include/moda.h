@@ -73,10 +73,10 @@ typedef enum { MODA_DTYPE_F32 = 0, MODA_DTYPE_BF16 = 1 } moda_dtype;
  * layer's depth memory is those S slots, in any order (the softmax does not depend on
  * the order of its keys).  A sliding window of the last C slots written is a ring:
  * the w-th write goes to slot w mod C (moda_depth_store_kv / moda_depth_project_kv),
- * and a reader passes S = min(writes so far, C).  The unread slots S .. C-1 get zero
- * weight; the tensor-core forward multiplies their value rows by that exact zero, so
- * they must hold finite numbers (zero a new buffer once).  moda_bwd sets dkd/dvd of
- * the unread slots to zero. */
+ * and a reader passes S = min(writes so far, C).  The unread slots S .. C-1 are never
+ * read (they may hold anything, NaN included, e.g. a ring's unwritten slots), so a
+ * half-full ring costs half the depth traffic; moda_bwd sets dkd/dvd of the unread
+ * slots to zero. */
 typedef struct {
   int32_t B, H, Hkv, T, S, d;
   int32_t dtype; /* moda_dtype */
@@ -86,11 +86,16 @@ typedef struct {
 
 /* Forward (the operation above).
  * In:  q, k, v, kd, vd (device, desc->dtype; kd/vd may be NULL when S == 0).
- * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it).
- * bf16 with d in {64, 128} runs on the tensor cores: tcgen05 MMAs with float32
- * accumulation for both memories (the depth slots of each query's position enter as
- * extra, block-masked key tiles of the same online softmax), P rounded to bf16 for the
- * PV products; float32 runs on the CUDA cores in float32. */
+ * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it); o must
+ * not overlap an input.
+ * bf16 with d in {64, 128}: one kernel in which the causal sequence keys run on the
+ * tensor cores (tcgen05 MMAs, float32 accumulation, P rounded to bf16 for the PV
+ * products) while warps of their own fold the depth slots of each query's position on
+ * the CUDA cores (float32 scores and sums, one read of each slab for the G heads); the
+ * two online-softmax states are joined by the online update rule and divided once by
+ * the joint denominator.  The depth part reaches the join through the rows of o,
+ * divided by its own partial sum and rounded to bf16, before o is overwritten with the
+ * result.  float32 runs on the CUDA cores in float32. */
 moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, void* o, float* lse, void* stream);
 
@@ -108,7 +113,10 @@ size_t moda_bwd_workspace_bytes(const moda_desc* desc);
  * Out: dq, dk, dv, dkd, dvd (device, desc->dtype; dkd/dvd may be NULL when S == 0).
  * workspace: device scratch of at least moda_bwd_workspace_bytes(desc) bytes,
  * 256-byte aligned; its contents on entry do not matter.  Calls that share a
- * workspace must not overlap on the GPU. */
+ * workspace must not overlap on the GPU.
+ * bf16 with d in {64, 128} and G = H / Hkv <= 8 runs on the tensor cores (the depth
+ * slots on the CUDA cores); G > 8 (and float32) runs every part on the CUDA cores,
+ * which is correct but several times slower. */
 moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                      void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream);
@@ -191,9 +199,11 @@ moda_status moda_depth_project_kv(const moda_desc* desc, int32_t slot, int32_t d
  * library's device image; nothing is allocated.  Problems whose
  * moda_bwd_workspace_bytes exceeds that size return MODA_ERR_WORKSPACE without
  * launching.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) and must therefore precede any stream capture on that
- * device.  Every call shares the array: calls that overlap on the GPU race and must
- * be serialised by the caller. */
+ * (cudaGetSymbolAddress) and caches it, so that first call should precede any stream
+ * capture on that device; after a cudaDeviceReset of a device the cached address is no
+ * longer valid and this entry point must not be called on that device again.  Every
+ * call shares the array: calls that overlap on the GPU race and must be serialised by
+ * the caller. */
 moda_status moda_bwd_noalloc(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                              const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                              void* dv, void* dkd, void* dvd, void* stream);

@@ -15,11 +15,15 @@
 // box walks the G heads fastest.
 //
 // Key tiles of a query tile t, in the order the online softmax takes them:
-//   depth tiles i = 0 .. n_d-1: 128 consecutive rows of the depth slabs of the tile's
-//     positions, kd[b, g, p0 + t*P + kappa/S, kappa%S, :] for kappa = 128 i .. 128 i + 127
-//     (the slabs of consecutive positions are contiguous); row r sees only the S keys of
-//     its own position, kappa in [(r/G) S, (r/G) S + S).  This is the same-position
-//     depth memory H_l of the slides' formulas, scored by the same MMA as the sequence.
+//   depth tiles i = 0 .. n_d-1.  When every slot in memory is read (S_read = S), 128
+//     consecutive rows of the tile's positions' slabs (contiguous in memory):
+//     kd[b, g, p0 + t*P + kappa/S, kappa%S, :] for kappa = 128 i .. 128 i + 127, and row r
+//     sees kappa in [(r/G) S, (r/G) S + S).  Otherwise (a bounded slot buffer read in part)
+//     the S_read slots of the dpt = floor(128 / S_read) positions p0 + t*P + i*dpt .. + dpt
+//     - 1, one 3-D TMA box (channels, slots, positions), so key kappa is slot kappa %
+//     S_read of position i*dpt + kappa / S_read: slots not read are never loaded.  This is
+//     the same-position depth memory H_l of the slides' formulas, scored by the same MMA as
+//     the sequence.
 //   sequence tiles j = 0 .. : keys 128 j .. 128 j + 127 of kv head g, causal mask.
 // Both kinds go through the same running max m and denominator l, the shared
 // online-softmax state of frame "Shared online-softmax states preserve the joint
@@ -95,11 +99,13 @@ struct FwdCfg {
 
 struct FwdTcParams {
   int B, H, Hkv, T, S, G, P;
-  int S_read;   // slots read per position (the rest of the S in memory get P = 0)
+  int S_read;   // slots read per position (the S - S_read others are never loaded)
   int n_pb;     // position blocks (of 2P positions) per (b, kv head)
   int n_units;  // B * Hkv * n_pb
   int n_cta;    // persistent CTAs
-  int n_d;      // depth key tiles per query tile: ceil(P*S / 128)
+  int packed;   // 1: every slot is read, depth keys packed over positions (2-D rows)
+  int dpt;      // positions per depth key tile when not packed: floor(128 / S_read)
+  int n_d;      // depth key tiles per query tile: ceil(P*S / 128) packed, else ceil(P / dpt)
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -220,6 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  if (p.n_d > 0 && !p.packed && p.dpt * p.S_read < BN) {
+    // rows of a depth key tile past its dpt * S_read keys are seen by no row, but enter
+    // the P V product with P = 0: they must hold finite numbers, so the ring starts zeroed
+    // (afterwards they hold loaded keys and values)
+    for (int i = threadIdx.x; i < C::NSLOT * C::TILE_BYTES / 16; i += kThreads)
+      st_shared_v4(sbase + C::OFF_KV + i * 16, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -257,16 +271,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* dst = smem + C::OFF_KV + slot * C::TILE_BYTES;
           uint64_t* full = &kv_full[2 * slot + (use & 1)];
-          mbar_arrive_expect_tx(full, C::TILE_BYTES);
           if (r < u.nd_items) {
-            // depth step i: K of each query tile, then V of each
+            // depth step i: K of each query tile, then V of each; rows past dpt*S_read keep
+            // what the slot held (finite: zeroed at start, then loaded keys and values) and
+            // are seen by no row
             const int i = r / (2 * two), w = r % (2 * two);
             const int kind = w / two, t = w % two;
-            const int row = (u.bg * p.T + u.p0 + t * p.P) * p.S + i * BN;
             const CUtensorMap* map = kind ? &tmVd : &tmKd;
+            if (p.packed) {
+              const int row = (u.bg * p.T + u.p0 + t * p.P) * p.S + i * BN;
+              mbar_arrive_expect_tx(full, C::TILE_BYTES);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * (BN * 128), map, full, h * 64, row);
+              for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * (BN * 128), map, full, h * 64, row);
+            } else {
+              const int pos0 = u.bg * p.T + u.p0 + t * p.P + i * p.dpt;
+              mbar_arrive_expect_tx(full, static_cast<uint32_t>(D) * p.S_read * p.dpt * 2);
+#pragma unroll
+              for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * (BN * 128), map, full, h * 64, 0, pos0);
+            }
           } else {
+            mbar_arrive_expect_tx(full, C::TILE_BYTES);
             const int j = (r - u.nd_items) >> 1, kind = (r - u.nd_items) & 1;
             const CUtensorMap* map = kind ? &tmV : &tmK;
 #pragma unroll
@@ -623,8 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool depth = j < p.n_d;
         int lo, hi;  // visible columns [lo, hi) of this row in this key tile
         if (depth) {
-          const int k0 = j * BN;
-          if (wp_hi * p.S + p.S_read <= k0 || wp_lo * p.S >= k0 + BN) {
+          // key offset of local position x in this depth tile: x * S - 128 j (packed) or
+          // (x - j dpt) S_read; visible when inside [0, 128) (packed) or x in the tile's dpt
+          const int d0 = j * p.dpt;  // first position of this depth tile (not packed)
+          const bool skip = p.packed ? (wp_hi * p.S + p.S <= j * BN || wp_lo * p.S >= j * BN + BN)
+                                     : (wp_hi < d0 || wp_lo >= d0 + p.dpt);
+          if (skip) {
             // no position of this warp has keys in this depth tile: P = 0
             if constexpr (C::SPLIT) {
               tc_fence_before();
@@ -646,8 +674,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++jcnt;
             continue;
           }
-          lo = valid ? pl * p.S - k0 : BN;
-          hi = valid ? lo + p.S_read : BN;
+          if (p.packed) {
+            lo = valid ? pl * p.S - j * BN : BN;
+            hi = valid ? lo + p.S : BN;
+          } else {
+            const bool in = valid && pl >= d0 && pl < d0 + p.dpt;
+            lo = in ? (pl - d0) * p.S_read : BN;
+            hi = in ? lo + p.S_read : BN;
+          }
         } else {
           const int kb = (j - p.n_d) * BN;
           lo = 0;
@@ -808,13 +842,24 @@ bool make_kv_map(CUtensorMap* map, const void* base, int D, int T, int groups) {
   return encode(map, base, 3, dims, strides, box);
 }
 
-// Depth slabs [B*Hkv*T*S rows][D] bf16 as a 2-D tensor; box 64 x 128 (128 consecutive
-// (position, slot) rows); rows past the end read as zeros.
-bool make_depth_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
+// Depth slabs [B*Hkv*T*S rows][D] bf16 as a 2-D tensor (every slot read); box 64 x 128
+// (128 consecutive (position, slot) rows); rows past the end read as zeros.
+bool make_depth_rows_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
   return encode(map, base, 2, dims, strides, box);
+}
+
+// Depth slabs [B*Hkv*T positions][C slots][D] bf16 as a 3-D tensor (D, S_read, positions):
+// slots from S_read on lie outside it and are never read; box 64 x S_read x dpt (the dpt
+// positions of a depth key tile); positions past the end read as zeros.
+bool make_depth_map(CUtensorMap* map, const void* base, int D, int S_read, int C, int64_t npos, int dpt) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S_read),
+                              static_cast<cuuint64_t>(npos)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(C) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(S_read), static_cast<cuuint32_t>(dpt)};
+  return encode(map, base, 3, dims, strides, box);
 }
 
 // Q [B][H][T][D] bf16 described as (D, H, T, B) -- heads before positions -- so that a
@@ -854,7 +899,9 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   p.n_cta = std::min(p.n_units, sms);
-  p.n_d = (p.P * pr.S + BN - 1) / BN;
+  p.packed = pr.S > 0 && pr.S_read == pr.S;
+  p.dpt = pr.S > 0 ? BN / pr.S_read : 1;
+  p.n_d = pr.S == 0 ? 0 : p.packed ? (p.P * pr.S + BN - 1) / BN : (p.P + p.dpt - 1) / p.dpt;
   p.scale_log2 = pr.scale_log2;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
@@ -864,8 +911,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
       !make_kv_map(&tv, a.v, D, pr.T, pr.B * pr.Hkv))
     return cudaErrorInvalidValue;
   if (pr.S > 0) {
-    const int64_t rows = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T * pr.S;
-    if (!make_depth_map(&tkd, a.kd, D, rows) || !make_depth_map(&tvd, a.vd, D, rows)) return cudaErrorInvalidValue;
+    const int64_t npos = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;
+    const bool okd = p.packed ? make_depth_rows_map(&tkd, a.kd, D, npos * pr.S) &&
+                                    make_depth_rows_map(&tvd, a.vd, D, npos * pr.S)
+                              : make_depth_map(&tkd, a.kd, D, pr.S_read, pr.S, npos, p.dpt) &&
+                                    make_depth_map(&tvd, a.vd, D, pr.S_read, pr.S, npos, p.dpt);
+    if (!okd) return cudaErrorInvalidValue;
   } else {
     tkd = tk;  // never read
     tvd = tv;
@@ -881,9 +932,11 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool fwd_sm103_supported(const Problem& p) {
-  // depth key rows are addressed with 32-bit TMA coordinates
-  const int64_t rows = static_cast<int64_t>(p.B) * p.Hkv * p.T * p.S;
-  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && rows < (int64_t(1) << 31);
+  // depth positions are addressed with 32-bit TMA coordinates; a position's read slots
+  // fit one depth key tile
+  const int64_t npos = static_cast<int64_t>(p.B) * p.Hkv * p.T;
+  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && npos * (p.S_read == p.S ? p.S : 1) < (int64_t(1) << 31) &&
+         (p.S == 0 || p.S_read <= BN);
 }
 
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {

@@ -55,11 +55,17 @@ def sample_positions(shape, n, seed):
 
 
 def sample_keys(shape, n, seed):
-    """Flat sequence keys (b*Hkv+g)*T+j; late keys are cheap for the oracle, plus a few early ones."""
+    """Flat sequence keys (b*Hkv+g)*T+j from three (b, kv head) pairs: the last keys (short
+    sums), the first keys j < 128 (the longest dK/dV sums, from the longest-running dK/dV
+    work), keys around the 128-key tile edges and random keys over the whole range."""
     rng = np.random.default_rng(seed)
     B, Hkv, T = shape.B, shape.Hkv, shape.T
-    b, g = rng.integers(B), rng.integers(Hkv)
-    base = (b * Hkv + g) * T
-    ks = [base + T - 1, base + T - 2, base + max(0, T - 130)] + [base + int(j) for j in rng.integers(T - 512 if T > 512 else 0, T, size=n)]
-    ks += [base + int(rng.integers(0, T))]
+    pairs = {(int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(3)}
+    ks = []
+    for b, g in sorted(pairs):
+        base = (b * Hkv + g) * T
+        js = {T - 1, T - 2, max(0, T - 130), 0, 1, min(T - 1, 127), min(T - 1, 128)}
+        js |= {int(j) for j in rng.integers(0, min(T, 128), size=2)}
+        js |= {int(j) for j in rng.integers(0, T, size=max(1, n // len(pairs)))}
+        ks += [base + j for j in js]
     return np.unique(np.array(ks, dtype=np.int64))

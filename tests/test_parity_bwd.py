@@ -90,3 +90,48 @@ def test_backward_full_size_sampled():
     tot = dk.double().sum(dim=2) + dkd.double().sum(dim=(2, 3))
     scale_ref = dk.double().abs().sum(dim=2)
     assert float((tot.abs() / scale_ref).max()) < 2e-2
+
+
+def test_ring_half_full_size_sampled():
+    """The training shape while a 32-slot ring is half full (16 slots read of 32 in memory),
+    forward and backward at full size on sampled rows, positions and keys; the unread half
+    of every position holds NaN, which must not reach any output."""
+    shape = WORKLOADS["bf16_train_ring_half"]
+    x = make_inputs(shape, seed=SEEDS["bf16_train_ring_half"], device="cuda", with_dout=True)
+    S, C = shape.S, shape.S_mem
+    x["kd"][:, :, :, S:] = float("nan")
+    x["vd"][:, :, :, S:] = float("nan")
+    o, lse = binding.moda_fwd(x["q"], x["k"], x["v"], x["kd"], x["vd"], slots=S)
+    dq, dk, dv, dkd, dvd = binding.moda_bwd(x["q"], x["k"], x["v"], x["kd"], x["vd"], o, lse, x["dout"], slots=S)
+    torch.cuda.synchronize()
+    assert binding.moda_device_status() == 0
+    for t in (o, lse, dq, dk, dv, dkd, dvd):
+        assert torch.isfinite(t.float()).all()
+    assert bool((dkd[:, :, :, S:] == 0).all()) and bool((dvd[:, :, :, S:] == 0).all())
+    read = {n: x[n][:, :, :, :S].contiguous() for n in ("kd", "vd")}
+    hx = [host_view(x[n]) if n not in read else host_view(read[n]) for n in NAMES]
+    from parity_util import TOL_OUT, max_abs, sample_rows
+
+    rows = sample_rows(shape, 24, seed=7)
+    ro, rl = oracle.forward(*hx[:5], rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    assert max_abs(as_f64(o.reshape(-1, shape.d)[idx]), ro) < TOL_OUT[shape.dtype]
+    assert max_abs(as_f64(lse.reshape(-1)[idx]), rl) < TOL_OUT[shape.dtype]
+    G, T = shape.G, shape.T
+    pos = sample_positions(shape, 12, seed=8)
+    rdq, rdkd, rdvd = oracle.backward_positions(*hx, positions=pos)
+    gdq, gdkd, gdvd = [], [], []
+    for p in pos:
+        t, bg = int(p % T), int(p // T)
+        b, g = bg // shape.Hkv, bg % shape.Hkv
+        gdq.append(as_f64(dq[b, g * G:(g + 1) * G, t]))
+        gdkd.append(as_f64(dkd[b, g, t, :S]))
+        gdvd.append(as_f64(dvd[b, g, t, :S]))
+    assert rel_err(np.stack(gdq), rdq) < TOL_GRAD_REL
+    assert rel_err(np.stack(gdkd), rdkd) < TOL_GRAD_REL
+    assert rel_err(np.stack(gdvd), rdvd) < TOL_GRAD_REL
+    keys = sample_keys(shape, 3, seed=9)
+    rdk, rdv = oracle.backward_keys(*hx, keys=keys)
+    kidx = torch.from_numpy(keys).cuda()
+    assert rel_err(as_f64(dk.reshape(-1, shape.d)[kidx]), rdk) < TOL_GRAD_REL
+    assert rel_err(as_f64(dv.reshape(-1, shape.d)[kidx]), rdv) < TOL_GRAD_REL

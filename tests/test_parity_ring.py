@@ -88,6 +88,48 @@ def test_ring_forward_backward(case):
             assert np.all(gg[:, :, :, unread] == 0.0), nm
 
 
+NAN_CASES = [
+    # name, B, H, Hkv, T, d, C (slots in memory), S read, dtype
+    ("bf16_d64_g4_half", 1, 8, 2, 300, 64, 32, 16, bf16),
+    ("bf16_d128_g1_third", 1, 4, 4, 257, 128, 24, 8, bf16),
+    ("bf16_d128_g4_one", 2, 8, 2, 200, 128, 8, 1, bf16),
+    ("fp32_d64_g2_half", 1, 4, 2, 100, 64, 6, 3, f32),
+]
+
+
+@pytest.mark.parametrize("case", NAN_CASES, ids=[c[0] for c in NAN_CASES])
+def test_unread_slots_holding_nan_and_inf_change_nothing(case):
+    """Slots S .. C-1 of a bounded slot buffer are outside the layer's depth memory: the
+    forward and the backward must not read them.  They are filled with NaN (keys) and
+    +/-Inf (values), which would poison any sum they entered, even with zero weight."""
+    name, B, H, Hkv, T, d, C, S, dt = case
+    shape = Shape(name, B, H, Hkv, T, d, S, dt, backward=True)
+    x = make_inputs(shape, seed=zlib.crc32(name.encode()) % 1000 + 71)
+    ring_k = torch.full((B, Hkv, T, C, d), float("nan"), dtype=dt)
+    ring_v = torch.full((B, Hkv, T, C, d), float("inf"), dtype=dt)
+    ring_v[..., ::2] = float("-inf")
+    ring_k[:, :, :, :S] = x["kd"]
+    ring_v[:, :, :, :S] = x["vd"]
+    g = {nm: x[nm].cuda() for nm in ("q", "k", "v", "dout")}
+    rk, rv = ring_k.cuda(), ring_v.cuda()
+    o, lse = binding.moda_fwd(g["q"], g["k"], g["v"], rk, rv, slots=S)
+    dq, dk, dv, dkd, dvd = binding.moda_bwd(g["q"], g["k"], g["v"], rk, rv, o, lse, g["dout"], slots=S)
+    torch.cuda.synchronize()
+    assert binding.moda_device_status() == 0
+    hx = [host_view(x[nm]) for nm in ("q", "k", "v", "kd", "vd", "dout")]
+    ro, rl = oracle.forward(*hx[:5])
+    assert np.isfinite(as_f64(o)).all() and np.isfinite(as_f64(lse)).all()
+    assert max_abs(as_f64(o), ro) < TOL_OUT[dt], max_abs(as_f64(o), ro)
+    assert max_abs(as_f64(lse), rl) < TOL_OUT[dt], max_abs(as_f64(lse), rl)
+    ref = oracle.backward(*hx)
+    for nm, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref[:3]):
+        assert rel_err(as_f64(got), r) < TOL_GRAD_REL, (nm, rel_err(as_f64(got), r))
+    for nm, got, r in (("dkd", dkd, ref[3]), ("dvd", dvd, ref[4])):
+        gg = as_f64(got)
+        assert rel_err(gg[:, :, :, :S], r) < TOL_GRAD_REL, (nm, rel_err(gg[:, :, :, :S], r))
+        assert np.all(gg[:, :, :, S:] == 0.0), nm
+
+
 @pytest.mark.parametrize("case", [c for c in CASES if c[-1] == bf16], ids=[c[0] for c in CASES if c[-1] == bf16])
 def test_ring_decode(case):
     """The decode step of the newest position reads the same ring (its slots [B,Hkv,C,d])."""
