@@ -86,16 +86,12 @@ typedef struct {
 
 /* Forward (the operation above).
  * In:  q, k, v, kd, vd (device, desc->dtype; kd/vd may be NULL when S == 0).
- * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it); o must
- * not overlap an input.
- * bf16 with d in {64, 128}: one kernel in which the causal sequence keys run on the
- * tensor cores (tcgen05 MMAs, float32 accumulation, P rounded to bf16 for the PV
- * products) while warps of their own fold the depth slots of each query's position on
- * the CUDA cores (float32 scores and sums, one read of each slab for the G heads); the
- * two online-softmax states are joined by the online update rule and divided once by
- * the joint denominator.  The depth part reaches the join through the rows of o,
- * divided by its own partial sum and rounded to bf16, before o is overwritten with the
- * result.  float32 runs on the CUDA cores in float32. */
+ * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it).
+ * bf16 with d in {64, 128} and S <= 128 runs on the tensor cores: tcgen05 MMAs with
+ * float32 accumulation for both memories (the depth slots read by each query's
+ * position enter as extra, block-masked key tiles of the same online softmax; slots
+ * not read are never loaded), P rounded to bf16 for the PV products; float32, and
+ * bf16 with S > 128, run on the CUDA cores in float32. */
 moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, void* o, float* lse, void* stream);
 
