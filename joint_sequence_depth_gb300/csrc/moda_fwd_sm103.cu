@@ -932,11 +932,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool fwd_sm103_supported(const Problem& p) {
-  // depth positions are addressed with 32-bit TMA coordinates; a position's read slots
-  // fit one depth key tile
+  // depth rows (all slots read) or positions (a part read) are addressed with 32-bit TMA
+  // coordinates; a position's read slots fit one depth key tile when only a part is read
   const int64_t npos = static_cast<int64_t>(p.B) * p.Hkv * p.T;
-  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && npos * (p.S_read == p.S ? p.S : 1) < (int64_t(1) << 31) &&
-         (p.S == 0 || p.S_read <= BN);
+  const bool packed = p.S_read == p.S;
+  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && npos * (packed ? p.S : 1) < (int64_t(1) << 31) &&
+         (p.S == 0 || packed || p.S_read <= BN);
 }
 
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {

@@ -14,7 +14,10 @@
 // use the array's name as a device address (on the host it names a stand-in), so
 // the first call on each device looks the device address up with
 // cudaGetSymbolAddress while that device is current and caches it; that first call
-// should therefore be made before any stream capture begins.  All calls share the
+// should therefore be made before any stream capture begins.  The cache lives as long
+// as the process: after cudaDeviceReset on a device the library's device image is
+// loaded again and may sit elsewhere, so a process that resets a device must not call
+// this entry point on it afterwards.  All calls share the
 // one array and it keeps whatever the previous call left in it; the backward
 // overwrites every word it reads, so nothing needs clearing.  Calls that overlap on
 // the GPU (different streams, or different host threads) race on the array.

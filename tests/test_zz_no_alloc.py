@@ -50,3 +50,46 @@ def test_noalloc_rejects_problems_beyond_its_array():
     assert binding.moda_bwd_workspace_bytes(big) > cap
     fake = [ctypes.c_void_p(1 << 20)] * 13
     assert lib.moda_bwd_noalloc(ctypes.byref(big), *fake, None) == 5  # MODA_ERR_WORKSPACE, nothing launched
+
+
+def _rows_at_cap(d):
+    """B*H*T rows whose workspace (row statistics, then the float32 dq share, each rounded
+    up to 256 bytes) is the largest that fits the array."""
+    cap = binding.moda_bwd_noalloc_max_workspace_bytes()
+    align = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    rows = cap // (8 + 4 * d)
+    while align(rows * 8) + align(rows * 4 * d) > cap:
+        rows -= 1
+    return rows
+
+
+def test_noalloc_at_its_capacity_and_one_row_over():
+    """A problem whose workspace fills the array to its last bytes (so an offset or rounding
+    error in the workspace layout would touch memory past it) matches moda_bwd with a normal
+    workspace on two calls in a row; one more row is refused before anything launches."""
+    d, H, Hkv, S = 64, 4, 1, 2
+    rows = _rows_at_cap(d)
+    assert rows % H == 0
+    T = rows // H
+    shape = Shape("at_cap", 1, H, Hkv, T, d, S, torch.bfloat16, backward=True)
+    desc = binding.make_desc(1, H, Hkv, T, S, d, torch.bfloat16)
+    cap = binding.moda_bwd_noalloc_max_workspace_bytes()
+    assert cap - 512 < binding.moda_bwd_workspace_bytes(desc) <= cap
+    x = make_inputs(shape, seed=78, device="cuda")
+    o, lse = binding.moda_fwd(x["q"], x["k"], x["v"], x["kd"], x["vd"])
+    ref = binding.moda_bwd(x["q"], x["k"], x["v"], x["kd"], x["vd"], o, lse, x["dout"])
+    torch.cuda.synchronize()
+    for _ in range(2):
+        grads = tuple(torch.full_like(t, float("nan")) for t in ref)
+        binding.moda_bwd_noalloc(x["q"], x["k"], x["v"], x["kd"], x["vd"], o, lse, x["dout"], grads)
+        torch.cuda.synchronize()
+        for nm, g, r in zip(("dq", "dk", "dv", "dkd", "dvd"), grads, ref):
+            ga, ra = as_f64(g), as_f64(r)
+            assert np.isfinite(ga).all(), nm
+            assert rel_err(ga, ra) < TOL_GRAD_REL, (nm, rel_err(ga, ra))
+    assert binding.moda_device_status() == 0
+    over = binding.make_desc(1, H, Hkv, T + 1, S, d, torch.bfloat16)
+    assert binding.moda_bwd_workspace_bytes(over) > cap
+    lib = binding.load_library()
+    fake = [ctypes.c_void_p(1 << 20)] * 13
+    assert lib.moda_bwd_noalloc(ctypes.byref(over), *fake, None) == 5  # MODA_ERR_WORKSPACE, nothing launched
