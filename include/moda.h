@@ -207,6 +207,74 @@ moda_status moda_bwd_noalloc(const moda_desc* desc, const void* q, const void* k
 /* Size in bytes of the fixed scratch array moda_bwd_noalloc uses. */
 size_t moda_bwd_noalloc_max_workspace_bytes(void);
 
+/* ---------------------------------------------------------------- context parallelism
+ * The pieces of a split of the positions 0 .. T-1 into chunks that live on different GPUs
+ * ("Mixture-of-Depths Attention", the future work of frame "The main open cost is
+ * retaining and reading depth history").  A query chunk's output is the joint softmax over
+ * the sequence keys of the chunks it sees and the depth slots of its own positions; the
+ * depth slots are read only by their own position (frame "Depth retrieval is restricted to
+ * the same token position"), so they never leave the GPU that holds the position.  Each
+ * (query chunk, key chunk) pair gives a partial state (O, lse) over that key chunk alone;
+ * moda_merge_partial combines the states by the online rule of frame "Shared
+ * online-softmax states preserve the joint operator".  Moving K/V between GPUs is the
+ * caller's (e.g. NCCL send/recv into its own device buffers); these calls read only local
+ * device memory.
+ *
+ * Chunk geometry (both moda_fwd_partial and moda_bwd_partial):
+ *   desc->T  query positions of the query chunk: q, o, dout, dq [B,H,T,d], lse [B,H,T];
+ *   desc->S  depth slots read with this key chunk: S > 0 in exactly one call per query
+ *            chunk (normally the pair of the chunk with itself), kd/vd/dkd/dvd
+ *            [B,Hkv,T,C,d] of the query chunk's own positions; S = 0 otherwise (kd, vd,
+ *            dkd, dvd may be NULL);
+ *   Tk       positions of the key chunk: k, v, dk_acc, dv_acc [B,Hkv,Tk,d];
+ *   delta    first query position minus first key position: key j of the chunk is visible
+ *            to query t of the chunk iff j <= t + delta.  0 <= delta and 1 <= Tk <= T + delta
+ *            (every query sees key 0, the last query sees every key), else
+ *            MODA_ERR_INVALID_ARG.  A chunk with itself: Tk = T, delta = 0 (moda_fwd's causal
+ *            mask).  A key chunk that ends before the query chunk starts: delta >= Tk - 1,
+ *            every key visible.  Pairs whose key chunk starts after the query chunk's
+ *            first position are not called (their keys are causally invisible).
+ * Errors, alignment, streams and ownership as for moda_fwd / moda_bwd. */
+
+/* Partial forward: o (desc->dtype) and lse (float32, required) of the query chunk over
+ * the visible keys of this key chunk (and the depth slots when S > 0) alone, normalised
+ * over those keys. */
+moda_status moda_fwd_partial(const moda_desc* desc, int32_t Tk, int32_t delta, const void* q, const void* k,
+                             const void* v, const void* kd, const void* vd, void* o, float* lse, void* stream);
+
+/* Merge of one partial state into a running state, rows = B*H*T of desc (d, dtype from desc):
+ *     m = max(lse_acc, lse_part),  w_a = e^{lse_acc - m},  w_b = e^{lse_part - m}
+ *     o_acc = (w_a o_acc + w_b o_part) / (w_a + w_b),   lse_acc = m + ln(w_a + w_b)
+ * o_acc [B,H,T,d] and lse_acc [B,H,T] are float32 and updated in place; o_part
+ * (desc->dtype) and lse_part (float32) are one moda_fwd_partial output.  first != 0 sets
+ * the running state to the partial one (o_acc, lse_acc are not read).  o_out (desc->dtype,
+ * may be NULL) receives the merged o_acc.  Once every visible key chunk is merged, o_acc
+ * and lse_acc are moda_fwd's o and lse of the query chunk (in float32, up to rounding; the
+ * order of the merges does not matter).  One elementwise kernel. */
+moda_status moda_merge_partial(const moda_desc* desc, float* o_acc, float* lse_acc, const void* o_part,
+                               const float* lse_part, int32_t first, void* o_out, void* stream);
+
+/* Partial backward of one (query chunk, key chunk) pair, with the Tk, delta and S of its
+ * moda_fwd_partial call.  o and lse are the query chunk's MERGED output and lse (over
+ * every key chunk), dout the gradient of o.  Adds this pair's share of the gradients, in
+ * float32:
+ *     dq_acc [B,H,T,d]          += dq of the query chunk through this key chunk (and the
+ *                                  depth slots when S > 0)
+ *     dk_acc, dv_acc [B,Hkv,Tk,d] += dk, dv of the key chunk from this query chunk's rows
+ * and, when S > 0, writes dkd, dvd (desc->dtype) of the query chunk's depth slots whole
+ * (only their own position's rows see them).  Summed over every pair, dq_acc, dk_acc and
+ * dv_acc are moda_bwd's dq, dk, dv in float32 (moda_convert_f32 rounds them).  workspace:
+ * at least moda_bwd_workspace_bytes(desc), as for moda_bwd. */
+moda_status moda_bwd_partial(const moda_desc* desc, int32_t Tk, int32_t delta, const void* q, const void* k,
+                             const void* v, const void* kd, const void* vd, const void* o, const float* lse,
+                             const void* dout, float* dq_acc, float* dk_acc, float* dv_acc, void* dkd, void* dvd,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* dst[i] = src[i] rounded to dtype (MODA_DTYPE_BF16: round to nearest even; MODA_DTYPE_F32:
+ * a copy) for i < n; src float32, both device, 16-byte aligned.  One elementwise kernel
+ * (none when n = 0). */
+moda_status moda_convert_f32(int64_t n, const float* src, int32_t dtype, void* dst, void* stream);
+
 /* Reads the device status word that bounded waits write (MODA_OK when clean) and,
  * when `clear` is non-zero, resets it.  Waits for `stream` first. */
 moda_status moda_device_status(int clear, void* stream);

@@ -28,7 +28,8 @@ EXPORTS = ("moda_fwd", "moda_bwd", "moda_bwd_workspace_bytes", "moda_device_stat
            "moda_status_str",
            "moda_version", "moda_launch_count", "moda_bwd_noalloc", "moda_bwd_noalloc_max_workspace_bytes",
            "moda_bwd_profiled", "moda_selftest_wait_timeout", "moda_decode", "moda_decode_workspace_bytes",
-           "moda_depth_store_kv", "moda_depth_project_kv")
+           "moda_depth_store_kv", "moda_depth_project_kv", "moda_fwd_partial", "moda_merge_partial",
+           "moda_bwd_partial", "moda_convert_f32")
 
 
 class MODAError(RuntimeError):
@@ -86,6 +87,15 @@ def load_library():
             lib.moda_depth_project_kv.argtypes = [d, ctypes.c_int32, ctypes.c_int32] + [p] * 6
             lib.moda_depth_project_kv.restype = ctypes.c_int
             lib.moda_decode.restype = ctypes.c_int
+            i32 = ctypes.c_int32
+            lib.moda_fwd_partial.argtypes = [d, i32, i32] + [p] * 8
+            lib.moda_fwd_partial.restype = ctypes.c_int
+            lib.moda_merge_partial.argtypes = [d, p, p, p, p, i32, p, p]
+            lib.moda_merge_partial.restype = ctypes.c_int
+            lib.moda_bwd_partial.argtypes = [d, i32, i32] + [p] * 14 + [ctypes.c_size_t, p]
+            lib.moda_bwd_partial.restype = ctypes.c_int
+            lib.moda_convert_f32.argtypes = [ctypes.c_int64, p, i32, p, p]
+            lib.moda_convert_f32.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -279,3 +289,97 @@ def moda_depth_project_kv(x, wk, wv, kd, vd, slot, stream=None):
     if st != MODA_OK:
         raise MODAError(st, "moda_depth_project_kv")
     return kd, vd
+
+
+# ---------------------------------------------------------------- context parallelism
+def _chunk_desc(q, k, kd, scale, slots):
+    """Description of a (query chunk, key chunk) pair: T from q, Tk from k."""
+    desc = _desc_from(q, k, kd, scale, slots)
+    B, H, T, d = q.shape
+    if k.shape[0] != B or k.shape[3] != d or k.dtype != q.dtype:
+        raise ValueError("k: batch, head dim and dtype must match q")
+    return desc, int(k.shape[2])
+
+
+def moda_fwd_partial(q, k, v, kd, vd, delta, o=None, lse=None, scale=None, stream=None, slots=None):
+    """Partial forward of a query chunk q[B,H,T,d] against a key chunk k, v[B,Hkv,Tk,d]
+    (moda_fwd_partial in include/moda.h): key j visible to query t iff j <= t + delta;
+    kd/vd (the query chunk's own depth slots) or None.  Returns (o, lse) over this chunk's
+    keys alone."""
+    desc, Tk = _chunk_desc(q, k, kd, scale, slots)
+    B, H, T, d = q.shape
+    _check_like(v, q.dtype, k.shape, "v")
+    if desc.S:
+        for t, name in ((kd, "kd"), (vd, "vd")):
+            _check_like(t, q.dtype, (B, desc.Hkv, T, _mem_slots(desc), d), name)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    st = load_library().moda_fwd_partial(ctypes.byref(desc), int(Tk), int(delta), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(kd) if desc.S else None, _ptr(vd) if desc.S else None, _ptr(o),
+                                         _ptr(lse), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_fwd_partial")
+    return o, lse
+
+
+def moda_merge_partial(o_acc, lse_acc, o_part, lse_part, first=False, o_out=None, stream=None):
+    """Merges a partial state (o_part [B,H,T,d], lse_part [B,H,T]) into the float32 running
+    state (o_acc, lse_acc) in place (moda_merge_partial in include/moda.h); ``o_out``
+    (o_part's dtype) optionally receives the merged O.  Returns (o_acc, lse_acc)."""
+    B, H, T, d = o_part.shape
+    _check_like(o_acc, torch.float32, o_part.shape, "o_acc")
+    _check_like(lse_acc, torch.float32, (B, H, T), "lse_acc")
+    _check_like(lse_part, torch.float32, (B, H, T), "lse_part")
+    if o_out is not None:
+        _check_like(o_out, o_part.dtype, o_part.shape, "o_out")
+    desc = make_desc(B, H, H, T, 0, d, o_part.dtype, None)
+    st = load_library().moda_merge_partial(ctypes.byref(desc), _ptr(o_acc), _ptr(lse_acc), _ptr(o_part),
+                                           _ptr(lse_part), 1 if first else 0, _ptr(o_out), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_merge_partial")
+    return o_acc, lse_acc
+
+
+def moda_bwd_partial(q, k, v, kd, vd, o, lse, dout, delta, dq_acc, dk_acc, dv_acc, dkd=None, dvd=None,
+                     workspace=None, scale=None, stream=None, slots=None):
+    """Adds one (query chunk, key chunk) pair's gradients to the float32 accumulators
+    dq_acc [B,H,T,d], dk_acc/dv_acc [B,Hkv,Tk,d] (moda_bwd_partial in include/moda.h); o,
+    lse are the query chunk's merged output and lse.  With depth slots (kd, vd not None)
+    dkd, dvd are written.  Returns (dq_acc, dk_acc, dv_acc, dkd, dvd)."""
+    desc, Tk = _chunk_desc(q, k, kd, scale, slots)
+    _check_like(dq_acc, torch.float32, q.shape, "dq_acc")
+    _check_like(dk_acc, torch.float32, k.shape, "dk_acc")
+    _check_like(dv_acc, torch.float32, k.shape, "dv_acc")
+    if desc.S:
+        if dkd is None:
+            dkd = torch.empty_like(kd)
+        if dvd is None:
+            dvd = torch.empty_like(vd)
+    need = moda_bwd_workspace_bytes(desc)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = load_library().moda_bwd_partial(
+        ctypes.byref(desc), int(Tk), int(delta), _ptr(q), _ptr(k), _ptr(v), _ptr(kd) if desc.S else None,
+        _ptr(vd) if desc.S else None, _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc),
+        _ptr(dkd) if desc.S else None, _ptr(dvd) if desc.S else None, _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_bwd_partial")
+    return dq_acc, dk_acc, dv_acc, dkd, dvd
+
+
+def moda_convert_f32(src, dtype, out=None, stream=None):
+    """Rounds a float32 tensor to ``dtype`` (torch.bfloat16 or torch.float32) in the library's
+    kernel (moda_convert_f32 in include/moda.h)."""
+    if src.dtype != torch.float32:
+        raise ValueError("src must be float32")
+    if out is None:
+        out = torch.empty(src.shape, dtype=dtype, device=src.device)
+    _check_like(out, dtype, src.shape, "out")
+    st = load_library().moda_convert_f32(ctypes.c_int64(src.numel()), _ptr(src), DTYPES[dtype], _ptr(out),
+                                         _stream(stream))
+    if st != MODA_OK:
+        raise MODAError(st, "moda_convert_f32")
+    return out

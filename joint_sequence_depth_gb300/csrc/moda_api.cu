@@ -69,6 +69,8 @@ moda::Problem problem_of(const moda_desc* d) {
   p.H = d->H;
   p.Hkv = d->Hkv;
   p.T = d->T;
+  p.Tk = d->T;
+  p.delta = 0;
   p.S = d->S > 0 ? static_cast<int>(slots_in_memory(d)) : 0;  // memory stride (no depth when S = 0)
   p.S_read = d->S;
   p.d = d->d;
@@ -118,20 +120,33 @@ size_t dq_accum_bytes(const moda_desc* d) {
   return align256(size_t(d->B) * d->H * d->T * d->d * sizeof(float));
 }
 
-}  // namespace
+// A key range of Tk positions whose key j is visible to query position t iff
+// j <= t + delta: 0 <= delta, 1 <= Tk <= T + delta (every query sees key 0 and the last
+// query sees every key).  Sets the effective (Tk, delta) of `p`: delta is clamped to Tk,
+// which leaves every mask unchanged and keeps t + delta within 32 bits.
+moda_status check_chunk(const moda_desc* d, int32_t Tk, int32_t delta, moda::Problem& p) {
+  if (Tk < 1 || delta < 0) return MODA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(Tk) > static_cast<int64_t>(d->T) + delta) return MODA_ERR_INVALID_ARG;
+  if (mul_capped(mul_capped(mul_capped(d->B, d->Hkv), Tk), d->d) > kMaxElems) return MODA_ERR_INVALID_ARG;
+  const int32_t eff = delta < Tk ? delta : Tk;
+  if (static_cast<int64_t>(d->T) + eff >= (int64_t(1) << 31)) return MODA_ERR_UNSUPPORTED;
+  p.Tk = Tk;
+  p.delta = eff;
+  return MODA_OK;
+}
 
-extern "C" {
-
-moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
-                     const void* vd, void* o, float* lse, void* stream) {
+moda_status fwd_impl(const moda_desc* desc, int32_t Tk, int32_t delta, const void* q, const void* k,
+                     const void* v, const void* kd, const void* vd, void* o, float* lse, void* stream) {
   moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  moda::FwdArgs a;
+  a.p = problem_of(desc);
+  st = check_chunk(desc, Tk, delta, a.p);
   if (st != MODA_OK) return st;
   if (!q || !k || !v || !o) return MODA_ERR_INVALID_ARG;
   if (desc->S > 0 && (!kd || !vd)) return MODA_ERR_INVALID_ARG;
   for (const void* p : {q, k, v, kd, vd, static_cast<const void*>(o), static_cast<const void*>(lse)})
     if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
-  moda::FwdArgs a;
-  a.p = problem_of(desc);
   a.status = status_word();
   if (a.status == nullptr) return MODA_ERR_CUDA;
   a.q = q;
@@ -150,6 +165,22 @@ moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const 
   return finish(e, s);
 }
 
+}  // namespace
+
+extern "C" {
+
+moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                     const void* vd, void* o, float* lse, void* stream) {
+  if (desc == nullptr) return MODA_ERR_INVALID_ARG;
+  return fwd_impl(desc, desc->T, 0, q, k, v, kd, vd, o, lse, stream);
+}
+
+moda_status moda_fwd_partial(const moda_desc* desc, int32_t Tk, int32_t delta, const void* q, const void* k,
+                             const void* v, const void* kd, const void* vd, void* o, float* lse, void* stream) {
+  if (lse == nullptr) return MODA_ERR_INVALID_ARG;  // the merge needs every partial's lse
+  return fwd_impl(desc, Tk, delta, q, k, v, kd, vd, o, lse, stream);
+}
+
 size_t moda_bwd_workspace_bytes(const moda_desc* desc) {
   if (check_desc(desc) != MODA_OK) return 0;
   return stats_bytes(desc) + dq_accum_bytes(desc);
@@ -162,11 +193,22 @@ moda_status moda_bwd(const moda_desc* desc, const void* q, const void* k, const 
                            stream, nullptr, 0);
 }
 
-moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
-                              const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                              void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream,
-                              void** events, int32_t n_events) {
+}  // extern "C"
+
+namespace {
+
+// Backward of a chunk pair (Tk, delta as for check_chunk).  acc: dq/dk/dv are float32
+// accumulators added to (dq_acc [B,H,T,d], dk_acc/dv_acc [B,Hkv,Tk,d]) instead of
+// storage-type outputs.
+moda_status bwd_impl(const moda_desc* desc, int32_t Tk, int32_t delta, bool acc, const void* q, const void* k,
+                     const void* v, const void* kd, const void* vd, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, void* dkd, void* dvd, void* workspace,
+                     size_t workspace_bytes, void* stream, void** events, int32_t n_events) {
   moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  moda::BwdArgs a;
+  a.p = problem_of(desc);
+  st = check_chunk(desc, Tk, delta, a.p);
   if (st != MODA_OK) return st;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return MODA_ERR_INVALID_ARG;
   if (desc->S > 0 && (!kd || !vd || !dkd || !dvd)) return MODA_ERR_INVALID_ARG;
@@ -176,8 +218,6 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
     if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < moda_bwd_workspace_bytes(desc)) return MODA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MODA_ERR_INVALID_ARG;
-  moda::BwdArgs a;
-  a.p = problem_of(desc);
   a.status = status_word();
   if (a.status == nullptr) return MODA_ERR_CUDA;
   a.q = q;
@@ -188,9 +228,12 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
   a.o = o;
   a.lse = lse;
   a.dout = dout;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
+  a.dq = acc ? nullptr : dq;
+  a.dk = acc ? nullptr : dk;
+  a.dv = acc ? nullptr : dv;
+  a.dq_acc = acc ? static_cast<float*>(dq) : nullptr;
+  a.dk_acc = acc ? static_cast<float*>(dk) : nullptr;
+  a.dv_acc = acc ? static_cast<float*>(dv) : nullptr;
   a.dkd = desc->S > 0 ? dkd : nullptr;
   a.dvd = desc->S > 0 ? dvd : nullptr;
   a.events = events;
@@ -204,6 +247,57 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
   else
     e = moda::launch_bwd_simt(a, desc->dtype, s);
   return finish(e, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
+                              const void* vd, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                              void* dv, void* dkd, void* dvd, void* workspace, size_t workspace_bytes, void* stream,
+                              void** events, int32_t n_events) {
+  if (desc == nullptr) return MODA_ERR_INVALID_ARG;
+  return bwd_impl(desc, desc->T, 0, false, q, k, v, kd, vd, o, lse, dout, dq, dk, dv, dkd, dvd, workspace,
+                  workspace_bytes, stream, events, n_events);
+}
+
+moda_status moda_bwd_partial(const moda_desc* desc, int32_t Tk, int32_t delta, const void* q, const void* k,
+                             const void* v, const void* kd, const void* vd, const void* o, const float* lse,
+                             const void* dout, float* dq_acc, float* dk_acc, float* dv_acc, void* dkd, void* dvd,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(desc, Tk, delta, true, q, k, v, kd, vd, o, lse, dout, dq_acc, dk_acc, dv_acc, dkd, dvd,
+                  workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+moda_status moda_merge_partial(const moda_desc* desc, float* o_acc, float* lse_acc, const void* o_part,
+                               const float* lse_part, int32_t first, void* o_out, void* stream) {
+  moda_status st = check_desc(desc);
+  if (st != MODA_OK) return st;
+  if (!o_acc || !lse_acc || !o_part || !lse_part) return MODA_ERR_INVALID_ARG;
+  for (const void* p : {static_cast<const void*>(o_acc), static_cast<const void*>(lse_acc), o_part,
+                        static_cast<const void*>(lse_part), static_cast<const void*>(o_out)})
+    if (p && !aligned16(p)) return MODA_ERR_INVALID_ARG;
+  moda::MergeArgs a;
+  a.rows = static_cast<int64_t>(desc->B) * desc->H * desc->T;
+  a.d = desc->d;
+  a.first = first != 0;
+  a.o_acc = o_acc;
+  a.lse_acc = lse_acc;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.o_out = o_out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(moda::launch_merge(a, desc->dtype, s), s);
+}
+
+moda_status moda_convert_f32(int64_t n, const float* src, int32_t dtype, void* dst, void* stream) {
+  if (n < 0 || n > kMaxElems) return MODA_ERR_INVALID_ARG;
+  if (dtype != MODA_DTYPE_F32 && dtype != MODA_DTYPE_BF16) return MODA_ERR_UNSUPPORTED;
+  if (n == 0) return MODA_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MODA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(moda::launch_convert(n, src, dst, dtype, s), s);
 }
 
 size_t moda_decode_workspace_bytes(const moda_desc* desc) {

@@ -41,6 +41,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 struct BwdTcParams {
   int B, H, Hkv, T, S, G;
+  int Tk;     // keys per (b, kv head) in k/v
+  int delta;  // key j is visible to query position t iff j <= t + delta
   int S_read;  // slots read per position; dkd/dvd of slots S_read .. S-1 are written as zero
   float scale, scale_log2;
   const __nv_bfloat16 *q, *k, *v, *kd, *vd, *dout;
@@ -49,6 +51,7 @@ struct BwdTcParams {
   const __nv_bfloat16* o;  // forward output (Delta = dO . O)
   float* dq_accum;  // depth share of dq, float32 [B,H,T,d] (read by the dQ kernel when S > 0)
   __nv_bfloat16 *dq, *dk, *dv, *dkd, *dvd;
+  float *dq_acc, *dk_acc, *dv_acc;  // set: dq/dk/dv are added to these in float32 instead
   int* status;
 };
 
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int p0 = pb * P;
   const int p_last = min(p0 + P, p.T) - 1;
-  const int n_kv = p_last / QBN + 1;
+  const int n_kv = min((p_last + p.delta) / QBN + 1, (p.Tk + QBN - 1) / QBN);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
@@ -516,6 +519,7 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
     const float nlse2 = st.x;  // -lse * log2(e)
     const float dlt = st.y;
     const float sl2 = p.scale_log2;
+    const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int bf = j % NBUF;
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
         const int c0 = wg * NCOL + hf * 32;  // first key column of this group
         uint32_t s[32], dpv[32];
         tmem_ld32x2(tmem + lane_base + C::TM_S + bf * QBN + c0, tmem + lane_base + C::TM_DP + bf * QBN + c0, s, dpv);
-        const int lim = valid ? pos - (j * QBN + c0) : -1;  // columns c <= lim are visible
+        const int lim = valid ? key_end - (j * QBN + c0) : -1;  // columns c <= lim are visible
         float e[32];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
@@ -583,7 +587,18 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
 #pragma unroll
             for (int i = 0; i < 32; ++i) extra[i] = 0.f;
           }
-          if (valid) {
+          if (valid && p.dq_acc != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 y = dst[i];
+              y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
+              y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
+              y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
+              y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
+              dst[i] = y;
+            }
+          } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -661,7 +676,9 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   const int bg = static_cast<int>(blockIdx.x) % ngroups;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int kb = kblk * KBM;
-  const int qt0 = kb / Pq, qt1 = (p.T - 1) / Pq;
+  // first query tile whose rows see key kb: position kb - delta (every key of the range is
+  // seen by position T - 1, so qt0 <= qt1)
+  const int qt0 = max(kb - p.delta, 0) / Pq, qt1 = (p.T - 1) / Pq;
   const int n_q = qt1 - qt0 + 1;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -846,7 +863,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       const int st = i % C::NSTAGE;
       const float4* sl = stat + st * (KBN / 2);
       const int p0 = (qt0 + i) * Pq;
-      const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
+      const bool diag = p0 + p.delta < kb + KBM;  // some rows of this tile precede some keys
       // P^T of this warpgroup's columns from S^T first, while dP^T may still be computed
       float e[NCOL];
 #pragma unroll
@@ -863,8 +880,8 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
           ee[c + 1] = ex2(ee[c + 1]);
         }
         if (diag) {
-          // row r sits at position p0 + r % Pq (head-major tile); keys after it are masked
-          const int dk = key - p0;
+          // row r sits at position p0 + r % Pq (head-major tile); keys after it (+ delta) are masked
+          const int dk = key - p.delta - p0;
           if ((Pq & (Pq - 1)) == 0) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) ee[c] = (dk > ((c0 + c) & (Pq - 1))) ? 0.f : ee[c];
@@ -915,14 +932,26 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
         for (int part = 0; part < 2; ++part) {
           if (NWG == 2 && part != wg) continue;
           const uint32_t src = part == 0 ? C::TM_DV : C::TM_DK;
-          __nv_bfloat16* out =
-              (part == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
+          const int64_t orow = (static_cast<int64_t>(bg) * p.Tk + (key < p.Tk ? key : 0)) * D;
+          __nv_bfloat16* out = (part == 0 ? p.dv : p.dk) + orow;
+          float* out_acc = p.dk_acc != nullptr ? (part == 0 ? p.dv_acc : p.dk_acc) + orow : nullptr;
           const float mul = part == 0 ? 1.f : p.scale;
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t acc[32];
             tmem_ld32(tmem + lane_base + src + c0, acc);
-            if (key < p.T) {
+            if (key < p.Tk && out_acc != nullptr) {
+              float4* dst = reinterpret_cast<float4*>(out_acc + c0);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                float4 y = dst[u];
+                y.x = fmaf(__uint_as_float(acc[4 * u]), mul, y.x);
+                y.y = fmaf(__uint_as_float(acc[4 * u + 1]), mul, y.y);
+                y.z = fmaf(__uint_as_float(acc[4 * u + 2]), mul, y.z);
+                y.w = fmaf(__uint_as_float(acc[4 * u + 3]), mul, y.w);
+                dst[u] = y;
+              }
+            } else if (key < p.Tk) {
               uint4* dst = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
               for (int u = 0; u < 4; ++u)
@@ -1001,7 +1030,7 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
   const int bg = static_cast<int>(blockIdx.x) % ngroups;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int kb = kblk * KBM;
-  const int qt0 = kb / P2, qt1 = (p.T - 1) / P2;
+  const int qt0 = max(kb - p.delta, 0) / P2, qt1 = (p.T - 1) / P2;
   const int n_q = qt1 - qt0 + 1;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -1192,8 +1221,8 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
       const int st = i % C::NSTAGE;
       const float4* sl = stat + st * (K2N / 2);  // [0, 32): -lse2 of rows 4c..4c+3; [32, 64): Delta
       const int p0 = (qt0 + i) * P2;
-      const bool diag = p0 < kb + KBM;  // some rows of this tile precede some keys
-      const int dk = key - p0;
+      const bool diag = p0 + p.delta < kb + KBM;  // some rows of this tile precede some keys
+      const int dk = key - p.delta - p0;
       // P^T and dS^T of both 32-column halves first, in registers; only then wait until the
       // dV/dK products of tile i-1 have read the single P^T, dS^T buffer (their commit
       // completes tile i-1's phase of q_empty), so that wait overlaps this tile's arithmetic
@@ -1259,13 +1288,26 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
         tc_fence_after();
         // dV (warpgroup 0) and dK (scaled; warpgroup 1)
         const uint32_t src = wg == 0 ? C::TM_DV : C::TM_DK;
-        __nv_bfloat16* out = (wg == 0 ? p.dv : p.dk) + (static_cast<int64_t>(bg) * p.T + (key < p.T ? key : 0)) * D;
+        const int64_t orow = (static_cast<int64_t>(bg) * p.Tk + (key < p.Tk ? key : 0)) * D;
+        __nv_bfloat16* out = (wg == 0 ? p.dv : p.dk) + orow;
+        float* out_acc = p.dk_acc != nullptr ? (wg == 0 ? p.dv_acc : p.dk_acc) + orow : nullptr;
         const float mul = wg == 0 ? 1.f : p.scale;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t acc[32];
           tmem_ld32(tmem + lane_base + src + c0, acc);
-          if (key < p.T) {
+          if (key < p.Tk && out_acc != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(out_acc + c0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 y = dst[u];
+              y.x = fmaf(__uint_as_float(acc[4 * u]), mul, y.x);
+              y.y = fmaf(__uint_as_float(acc[4 * u + 1]), mul, y.y);
+              y.z = fmaf(__uint_as_float(acc[4 * u + 2]), mul, y.z);
+              y.w = fmaf(__uint_as_float(acc[4 * u + 3]), mul, y.w);
+              dst[u] = y;
+            }
+          } else if (key < p.Tk) {
             uint4* dst = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -1340,7 +1382,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int p0 = pb * P;
   const int p_last = min(p0 + P, p.T) - 1;
-  const int n_kv = p_last / Q2N + 1;
+  const int n_kv = min((p_last + p.delta) / Q2N + 1, (p.Tk + Q2N - 1) / Q2N);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
@@ -1512,6 +1554,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     const float nlse2 = stt.x;  // -lse * log2(e)
     const float dlt = stt.y;
     const float sl2 = p.scale_log2;
+    const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = warp_wait(s_full, j & 1, abort_flag);
@@ -1531,7 +1574,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
           e[c] = ex2(e[c]);
           e[c + 1] = ex2(e[c + 1]);
         }
-        const int lim = valid ? pos - (j * Q2N + wg * 64) : -1;  // columns c <= lim are visible
+        const int lim = valid ? key_end - (j * Q2N + wg * 64) : -1;  // columns c <= lim are visible
         if (lim < 63) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
@@ -1598,7 +1641,18 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) extra[i] = 0.f;
         }
-        if (valid) {
+        if (valid && p.dq_acc != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 y = dst[i];
+            y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
+            y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
+            y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
+            y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
+            dst[i] = y;
+          }
+        } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -1652,6 +1706,8 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.H = pr.H;
   p.Hkv = pr.Hkv;
   p.T = pr.T;
+  p.Tk = pr.Tk;
+  p.delta = pr.delta;
   p.S = pr.S;
   p.S_read = pr.S_read;
   p.G = pr.G;
@@ -1672,6 +1728,9 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.dkd = static_cast<__nv_bfloat16*>(a.dkd);
   p.dvd = static_cast<__nv_bfloat16*>(a.dvd);
+  p.dq_acc = a.dq_acc;
+  p.dk_acc = a.dk_acc;
+  p.dv_acc = a.dv_acc;
   p.status = a.status;
 
   // stage 0: Delta (its own kernel only when S = 0; otherwise the depth kernel forms the
@@ -1698,11 +1757,11 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap tk128, tv128, tk64, tv64, tq, to;
   const int planes_kv = pr.B * pr.Hkv, planes_q = pr.B * pr.H;
   const int pq = KBN / pr.G;
-  if (!make_map(&tk128, a.k, D, pr.T, planes_kv, KBM, 1) || !make_map(&tv128, a.v, D, pr.T, planes_kv, KBM, 1) ||
-      !make_map(&tk64, a.k, D, pr.T, planes_kv, QBN, 1) || !make_map(&tv64, a.v, D, pr.T, planes_kv, QBN, 1) ||
+  if (!make_map(&tk128, a.k, D, pr.Tk, planes_kv, KBM, 1) || !make_map(&tv128, a.v, D, pr.Tk, planes_kv, KBM, 1) ||
+      !make_map(&tk64, a.k, D, pr.Tk, planes_kv, QBN, 1) || !make_map(&tv64, a.v, D, pr.Tk, planes_kv, QBN, 1) ||
       !make_map(&tq, a.q, D, pr.T, planes_q, pq, pr.G) || !make_map(&to, a.dout, D, pr.T, planes_q, pq, pr.G))
     return cudaErrorInvalidValue;
-  const unsigned grid_kv = static_cast<unsigned>((pr.T + KBM - 1) / KBM) * planes_kv;
+  const unsigned grid_kv = static_cast<unsigned>((pr.Tk + KBM - 1) / KBM) * planes_kv;
   const int P = QBM / pr.G;
   const unsigned grid_q = static_cast<unsigned>((pr.T + P - 1) / P) * planes_kv;
   if constexpr (D == 64) {

@@ -21,6 +21,8 @@ constexpr int kStatusTimeout = 4;  // a bounded wait ran out (MODA_ERR_TIMEOUT)
 
 struct Problem {
   int B, H, Hkv, T;
+  int Tk;      // key positions per (b, kv head) in k/v (T for a whole sequence)
+  int delta;   // key j is visible to query position t iff j <= t + delta (0 for a whole sequence)
   int S;       // depth slots per position in kd/vd memory (0: no depth memory)
   int S_read;  // slots 0 .. S_read-1 of each position are read (S_read <= S; S_read = 0 iff S = 0)
   int d, G;
@@ -44,6 +46,9 @@ struct BwdArgs {
   void *dq, *dk, *dv, *dkd, *dvd;
   float2* stats;    // workspace [B,H,T]: {-lse * log2(e), Delta_t = dout_t . o_t}
   float* dq_accum;  // workspace [B,H,T,d] float32 (tensor-core path)
+  // When set (all three), the sequence gradients are added in float32 to these instead
+  // of being written to dq/dk/dv: dq_acc [B,H,T,d], dk_acc/dv_acc [B,Hkv,Tk,d].
+  float *dq_acc, *dk_acc, *dv_acc;
   void** events;    // optional cudaEvent_t[n_events]: stage k recorded at events[2k] (start), [2k+1] (end)
   int n_events;
 };
@@ -67,6 +72,18 @@ struct DecodeSplit {
 
 // Depth-KV write path: slot `slot` of kd/vd [B,Hkv,T,S,d] from the attention KV
 // (k/v [B,Hkv,T,d]) or from the projection of x [B,T,Dm] by wk/wv [Dm, Hkv*d].
+// Merge of a partial forward state (o_part, lse_part) into a running float32 state
+// (o_acc, lse_acc), rows = B*H*T rows of d columns; `first`: the running state is set to
+// the partial one.  o_out (may be null) receives the merged O in the storage type.
+struct MergeArgs {
+  int64_t rows;
+  int d, first;
+  float *o_acc, *lse_acc;
+  const void* o_part;
+  const float* lse_part;
+  void* o_out;
+};
+
 struct DepthWriteArgs {
   int B, Hkv, T, S, d, slot, Dm;
   int* status;
@@ -131,5 +148,7 @@ cudaError_t launch_decode_sm103(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_depth_store_sm103(const DepthWriteArgs& a, cudaStream_t s);
 cudaError_t launch_depth_project_sm103(const DepthWriteArgs& a, cudaStream_t s);
 bool bwd_sm103_supported(const Problem& p);
+cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_convert(int64_t n, const float* src, void* dst, int dtype, cudaStream_t s);
 
 }  // namespace moda

@@ -24,7 +24,11 @@
 //     S_read of position i*dpt + kappa / S_read: slots not read are never loaded.  This is
 //     the same-position depth memory H_l of the slides' formulas, scored by the same MMA as
 //     the sequence.
-//   sequence tiles j = 0 .. : keys 128 j .. 128 j + 127 of kv head g, causal mask.
+//   sequence tiles j = 0 .. : keys 128 j .. 128 j + 127 of kv head g, causal mask: key
+//               j is visible to position t when j <= t + delta and j < Tk.  A whole
+//               sequence has delta = 0 and Tk = T; a query chunk scored against the key
+//               chunk of an earlier range of positions (context parallelism) has the
+//               offset delta = (first query position) - (first key position) > 0.
 // Both kinds go through the same running max m and denominator l, the shared
 // online-softmax state of frame "Shared online-softmax states preserve the joint
 // operator", and one PV accumulator O: the depth slots are never normalised apart.
@@ -99,6 +103,8 @@ struct FwdCfg {
 
 struct FwdTcParams {
   int B, H, Hkv, T, S, G, P;
+  int Tk;       // keys per (b, kv head) in k/v (T unless a key chunk of another range is read)
+  int delta;    // key j is visible to query position t iff j <= t + delta (0 <= delta)
   int S_read;   // slots read per position (the S - S_read others are never loaded)
   int n_pb;     // position blocks (of 2P positions) per (b, kv head)
   int n_units;  // B * Hkv * n_pb
@@ -137,8 +143,9 @@ __device__ __forceinline__ Unit unit_at(const FwdTcParams& p, int c, int k) {
   u.g = u.bg % p.Hkv;
   u.p0 = pb * 2 * p.P;
   const int end = min(u.p0 + 2 * p.P, p.T);
-  u.nt[0] = (min(u.p0 + p.P, p.T) - 1) / BN + 1;
-  u.nt[1] = (u.p0 + p.P < p.T) ? (end - 1) / BN + 1 : 0;
+  const int nk = (p.Tk + BN - 1) / BN;  // key tiles of the key range
+  u.nt[0] = min((min(u.p0 + p.P, p.T) - 1 + p.delta) / BN + 1, nk);
+  u.nt[1] = (u.p0 + p.P < p.T) ? min((end - 1 + p.delta) / BN + 1, nk) : 0;
   u.ns[0] = p.n_d + u.nt[0];
   u.ns[1] = u.nt[1] > 0 ? p.n_d + u.nt[1] : 0;
   u.nd_items = p.n_d * (u.nt[1] > 0 ? 4 : 2);
@@ -683,9 +690,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi = in ? lo + p.S_read : BN;
           }
         } else {
+          // keys kb + c with c < hi are visible: c <= pos + delta - kb and kb + c < Tk
           const int kb = (j - p.n_d) * BN;
           lo = 0;
-          hi = (kb + BN - 1 > pfirst || !valid) ? (valid ? pos - kb + 1 : 0) : BN;
+          hi = (kb + BN - 1 > pfirst + p.delta || kb + BN > p.Tk || !valid)
+                   ? (valid ? min(pos + p.delta - kb + 1, p.Tk - kb) : 0)
+                   : BN;
         }
         float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
         {
@@ -890,6 +900,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.H = pr.H;
   p.Hkv = pr.Hkv;
   p.T = pr.T;
+  p.Tk = pr.Tk;
+  p.delta = pr.delta;
   p.S = pr.S;
   p.S_read = pr.S_read;
   p.G = pr.G;
@@ -907,8 +919,8 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   p.lse = a.lse;
   p.status = a.status;
   CUtensorMap tq, tk, tv, tkd, tvd;
-  if (!make_q_map(&tq, a.q, D, pr.T, pr.H, pr.B, p.P, pr.G) || !make_kv_map(&tk, a.k, D, pr.T, pr.B * pr.Hkv) ||
-      !make_kv_map(&tv, a.v, D, pr.T, pr.B * pr.Hkv))
+  if (!make_q_map(&tq, a.q, D, pr.T, pr.H, pr.B, p.P, pr.G) || !make_kv_map(&tk, a.k, D, pr.Tk, pr.B * pr.Hkv) ||
+      !make_kv_map(&tv, a.v, D, pr.Tk, pr.B * pr.Hkv))
     return cudaErrorInvalidValue;
   if (pr.S > 0) {
     const int64_t npos = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;

@@ -11,7 +11,9 @@
 // Forward state per row follows the frame "Shared online-softmax states preserve
 // the joint operator": running max m, denominator acc, numerator o, updated key
 // by key over the causal sequence keys and then the S depth slots of the same
-// position, normalised once at the end.
+// position, normalised once at the end.  Key j is visible to position t when
+// j <= t + delta and j < Tk (delta = 0, Tk = T for a whole sequence; a key chunk of
+// an earlier range of positions has delta > 0).
 #include "moda_common.cuh"
 
 namespace moda {
@@ -58,6 +60,13 @@ __device__ __forceinline__ void store_frag(T* p, const float (&x)[N]) {
   for (int c = 0; c < N; ++c) p[c] = from_f32<T>(x[c]);
 }
 
+// Adds a fragment to a float32 accumulator (the accumulating backward of a chunk pair).
+template <int N>
+__device__ __forceinline__ void add_frag(float* p, const float (&x)[N]) {
+#pragma unroll
+  for (int c = 0; c < N; ++c) p[c] += x[c];
+}
+
 template <int N>
 __device__ __forceinline__ float dot(const float (&a)[N], const float (&b)[N]) {
   float s = 0.f;
@@ -92,8 +101,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const FwdArgs a) 
   const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H), g = h / p.G;
   const int64_t bg = static_cast<int64_t>(b) * p.Hkv + g;
   const T* q = static_cast<const T*>(a.q) + (bh * p.T + t) * D + lane * N;
-  const T* k = static_cast<const T*>(a.k) + bg * p.T * D + lane * N;
-  const T* v = static_cast<const T*>(a.v) + bg * p.T * D + lane * N;
+  const T* k = static_cast<const T*>(a.k) + bg * p.Tk * D + lane * N;
+  const T* v = static_cast<const T*>(a.v) + bg * p.Tk * D + lane * N;
+  const int j_end = min(t + p.delta, p.Tk - 1);  // last visible key
 
   float qf[N], kf[N], vf[N], o[N];
   load_frag(q, qf);
@@ -103,8 +113,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_simt_kernel(const FwdArgs a) 
     o[c] = 0.f;
   }
   float m = -INFINITY, acc = 0.f;
-  // causal sequence keys j <= t
-  for (int j = 0; j <= t; ++j) {
+  // causal sequence keys j <= t + delta (j < Tk)
+  for (int j = 0; j <= j_end; ++j) {
     load_frag(k + static_cast<int64_t>(j) * D, kf);
     const float s2 = warp_sum(dot(qf, kf));
     load_frag(v + static_cast<int64_t>(j) * D, vf);
@@ -158,8 +168,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(const BwdArgs 
   const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H), g = h / p.G;
   const int64_t bg = static_cast<int64_t>(b) * p.Hkv + g;
   const int64_t row = bh * p.T + t;
-  const T* k = static_cast<const T*>(a.k) + bg * p.T * D + lane * N;
-  const T* v = static_cast<const T*>(a.v) + bg * p.T * D + lane * N;
+  const T* k = static_cast<const T*>(a.k) + bg * p.Tk * D + lane * N;
+  const T* v = static_cast<const T*>(a.v) + bg * p.Tk * D + lane * N;
+  const int j_end = min(t + p.delta, p.Tk - 1);
   float qf[N], df[N], kf[N], vf[N], dq[N];
   load_frag(static_cast<const T*>(a.q) + row * D + lane * N, qf);
   load_frag(static_cast<const T*>(a.dout) + row * D + lane * N, df);
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(const BwdArgs 
   const float2 st = a.stats[row];
   const float lse2 = -st.x;
   const float Dt = st.y;
-  for (int j = 0; j <= t; ++j) {
+  for (int j = 0; j <= j_end; ++j) {
     load_frag(k + static_cast<int64_t>(j) * D, kf);
     load_frag(v + static_cast<int64_t>(j) * D, vf);
     const float pj = exp2f(warp_sum(dot(qf, kf)) - lse2);
@@ -194,28 +205,30 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_simt_kernel(const BwdArgs 
   }
 #pragma unroll
   for (int c = 0; c < N; ++c) dq[c] *= p.scale;
-  store_frag(static_cast<T*>(a.dq) + row * D + lane * N, dq);
+  if (a.dq_acc != nullptr) add_frag(a.dq_acc + row * D + lane * N, dq);
+  else store_frag(static_cast<T*>(a.dq) + row * D + lane * N, dq);
 }
 
-// dk, dv for one sequence key (b, g, j): every row t >= j of the G heads of g.
+// dk, dv for one sequence key (b, g, j): every row t >= j - delta of the G heads of g.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(const BwdArgs a) {
   constexpr int N = D / 32;
   const Problem& p = a.p;
   const int lane = threadIdx.x & 31;
-  const int tiles = (p.T + kWarps - 1) / kWarps;
+  const int tiles = (p.Tk + kWarps - 1) / kWarps;
   const int64_t bg = blockIdx.x / tiles;
   const int j = (blockIdx.x % tiles) * kWarps + (threadIdx.x >> 5);
-  if (j >= p.T) return;
+  if (j >= p.Tk) return;
   const int b = static_cast<int>(bg / p.Hkv), g = static_cast<int>(bg % p.Hkv);
+  const int t0 = max(j - p.delta, 0);  // first query position that sees key j
   float kf[N], vf[N], qf[N], df[N], dk[N], dv[N];
-  load_frag(static_cast<const T*>(a.k) + (bg * p.T + j) * D + lane * N, kf);
-  load_frag(static_cast<const T*>(a.v) + (bg * p.T + j) * D + lane * N, vf);
+  load_frag(static_cast<const T*>(a.k) + (bg * p.Tk + j) * D + lane * N, kf);
+  load_frag(static_cast<const T*>(a.v) + (bg * p.Tk + j) * D + lane * N, vf);
 #pragma unroll
   for (int c = 0; c < N; ++c) dk[c] = dv[c] = 0.f;
   for (int hh = 0; hh < p.G; ++hh) {
     const int64_t bh = static_cast<int64_t>(b) * p.H + g * p.G + hh;
-    for (int t = j; t < p.T; ++t) {
+    for (int t = t0; t < p.T; ++t) {
       const int64_t row = bh * p.T + t;
       load_frag(static_cast<const T*>(a.q) + row * D + lane * N, qf);
       load_frag(static_cast<const T*>(a.dout) + row * D + lane * N, df);
@@ -231,8 +244,13 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_simt_kernel(const BwdArg
   }
 #pragma unroll
   for (int c = 0; c < N; ++c) dk[c] *= p.scale;
-  store_frag(static_cast<T*>(a.dk) + (bg * p.T + j) * D + lane * N, dk);
-  store_frag(static_cast<T*>(a.dv) + (bg * p.T + j) * D + lane * N, dv);
+  if (a.dk_acc != nullptr) {
+    add_frag(a.dk_acc + (bg * p.Tk + j) * D + lane * N, dk);
+    add_frag(a.dv_acc + (bg * p.Tk + j) * D + lane * N, dv);
+  } else {
+    store_frag(static_cast<T*>(a.dk) + (bg * p.Tk + j) * D + lane * N, dk);
+    store_frag(static_cast<T*>(a.dv) + (bg * p.Tk + j) * D + lane * N, dv);
+  }
 }
 
 // dkd, dvd for one position (b, g, t): the G heads of g at position t.
@@ -302,7 +320,7 @@ cudaError_t bwd_simt(const BwdArgs& a, cudaStream_t s) {
         <<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
   mark_event(a, 3, s);
   mark_event(a, 4, s);
-  bwd_dkdv_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.T), kWarps * 32, 0, s>>>(a);
+  bwd_dkdv_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.Hkv, a.p.Tk), kWarps * 32, 0, s>>>(a);
   mark_event(a, 5, s);
   mark_event(a, 6, s);
   bwd_dq_simt_kernel<T, D><<<blocks_for(static_cast<int64_t>(a.p.B) * a.p.H, a.p.T), kWarps * 32, 0, s>>>(a);

@@ -143,3 +143,46 @@ def test_decode_rejects_bad_arguments(lib):
     bad = [f] * 6
     bad[3] = None  # depth keys missing while S > 0
     assert dec(desc(S=3), 0, bad) == 1
+
+
+def test_context_parallel_calls_reject_bad_arguments(lib):
+    """Chunk geometry (delta < 0, Tk < 1, Tk > T + delta), a missing lse, null or
+    misaligned pointers: refused before any launch.  T = 16 query positions."""
+    f = ctypes.c_void_p(FAKE)
+    d = desc()
+    # pointers: q, k, v, kd, vd, o, lse
+    fp = lambda Tk, delta, ptrs=None: lib.moda_fwd_partial(  # noqa: E731
+        ctypes.byref(d), Tk, delta, *(ptrs or [f] * 7), None)
+    assert fp(16, -1) == 1
+    assert fp(0, 0) == 1
+    assert fp(17, 0) == 1        # key 16 is seen by no query
+    assert fp(40, 23) == 1       # T + delta = 39 < 40
+    assert fp(16, 0, [f] * 6 + [None]) == 1  # lse required
+    for i in range(7):
+        bad = [f] * 7
+        bad[i] = ctypes.c_void_p(FAKE + 8)
+        assert fp(16, 0, bad) == 1
+    ws = ctypes.c_void_p(FAKE)
+    need = ctypes.c_size_t(lib.moda_bwd_workspace_bytes(ctypes.byref(d)))
+    bp = lambda Tk, delta, ptrs=None: lib.moda_bwd_partial(  # noqa: E731
+        ctypes.byref(d), Tk, delta, *(ptrs or [f] * 13), ws, need, None)
+    assert bp(16, -1) == 1
+    assert bp(17, 0) == 1
+    assert bp(16, 0, [f] * 9 + [None] + [f] * 3) == 1  # dk accumulator missing
+    assert lib.moda_bwd_partial(ctypes.byref(d), 16, 0, *([f] * 13), ws, ctypes.c_size_t(need.value - 1),
+                                None) == 5
+    mp = lambda ptrs, dd=d: lib.moda_merge_partial(ctypes.byref(dd), *ptrs[:4], 0, ptrs[4], None)  # noqa: E731
+    for i in range(4):
+        bad = [f] * 5
+        bad[i] = None
+        assert mp(bad) == 1
+    for i in range(5):
+        bad = [f] * 5
+        bad[i] = ctypes.c_void_p(FAKE + 4)
+        assert mp(bad) == 1
+    assert mp([f] * 5, desc(d=96)) == 2
+    cv = lib.moda_convert_f32
+    assert cv(ctypes.c_int64(-1), f, 1, f, None) == 1
+    assert cv(ctypes.c_int64(16), f, 7, f, None) == 2
+    assert cv(ctypes.c_int64(16), ctypes.c_void_p(FAKE + 4), 1, f, None) == 1
+    assert cv(ctypes.c_int64(0), None, 1, None, None) == 0  # nothing to do, nothing launched
