@@ -39,6 +39,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Key block and (b, kv head) of a dK/dV CTA.  CTAs run roughly in index order, so the
+// index walks the (b, kv head) groups in bands of kKvBand: inside a band the smallest key
+// blocks (most query tiles) come first, and the CTAs in flight at any time read the Q/dO
+// rows of at most a band or two of groups, which stay in L2 between their reads (a
+// group's Q and dO are read once by each of its key blocks).
+constexpr int kKvBand = 8;
+__device__ __forceinline__ void kv_block_of(int idx, int ngroups, int n_kblk, int& kblk, int& bg) {
+  const int full = ngroups / kKvBand;  // complete bands
+  if (idx < full * kKvBand * n_kblk) {
+    const int band = idx / (kKvBand * n_kblk), r = idx % (kKvBand * n_kblk);
+    kblk = r / kKvBand;
+    bg = band * kKvBand + r % kKvBand;
+  } else {
+    const int rest = ngroups - full * kKvBand, r = idx - full * kKvBand * n_kblk;
+    kblk = r / rest;
+    bg = full * kKvBand + r % rest;
+  }
+}
+
 struct BwdTcParams {
   int B, H, Hkv, T, S, G;
   int Tk;     // keys per (b, kv head) in k/v
@@ -672,8 +691,8 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Pq = KBN / p.G;  // positions per query tile
   const int ngroups = p.B * p.Hkv;
-  const int kblk = static_cast<int>(blockIdx.x) / ngroups;  // smallest key blocks (most query tiles) first
-  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  int kblk, bg;
+  kv_block_of(static_cast<int>(blockIdx.x), ngroups, (p.Tk + KBM - 1) / KBM, kblk, bg);
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int kb = kblk * KBM;
   // first query tile whose rows see key kb: position kb - delta (every key of the range is
@@ -985,15 +1004,16 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
 // as they have read them (s_free), so S^T and dP^T of tile i+1 are computed while P^T and
 // dS^T of tile i are formed; dV, dK of tile i follow (p_full), and their commit (q_empty)
 // frees both the Q/dO stage and P^T, dS^T.
-// Warps: 0 loads, 1 issues S^T and dP^T, 10 issues dV and dK, 2..9 gradient warps:
+// Warps: 0 loads, 1 issues S^T and dP^T, 10 issues dV, 11 issues dK, 2..9 gradient warps:
 // warpgroup w forms query columns [64w, 64w+64) of every tile; thread = key = TMEM lane.
-// Two issuing threads, so that one waiting on a barrier (Q/dO loads and S^T released;
-// P^T, dS^T written) does not leave the tensor pipe's short queue empty.
+// Three issuing threads: one waiting on a barrier (Q/dO loads and S^T released; P^T, dS^T
+// written) does not leave the tensor pipe's short queue empty, and the N = 64 gradient
+// products, which one thread issues more slowly than the pipe executes them, come from two.
 constexpr int K2N = 128;
 
 struct Dkv64Cfg {
   static constexpr int D = 64;
-  static constexpr int THREADS = 64 + 256 + 32;
+  static constexpr int THREADS = 64 + 256 + 64;
   static constexpr int KV_BYTES = KBM * D * 2;    // the CTA's K (or V) tile
   static constexpr int QT_BYTES = K2N * D * 2;    // one 128-row Q (or dO) tile
   static constexpr int NSTAGE = 4;
@@ -1003,8 +1023,8 @@ struct Dkv64Cfg {
   static constexpr int OFF_Q = 2 * KV_BYTES;      // stage s: Q at + s*STAGE, dO at + QT_BYTES
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][128] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * K2N * 8;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, drain_g, drain, last_done
-  static constexpr int NBAR = 1 + 2 * NSTAGE + 6;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full, s_free, p_full, drain_g[2], drain, last_done
+  static constexpr int NBAR = 1 + 2 * NSTAGE + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_P = 256, TM_DS = 320, TM_DV = 384, TM_DK = 448;
@@ -1026,8 +1046,8 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P2 = K2N / p.G;  // positions per query tile
   const int ngroups = p.B * p.Hkv;
-  const int kblk = static_cast<int>(blockIdx.x) / ngroups;  // smallest key blocks (most query tiles) first
-  const int bg = static_cast<int>(blockIdx.x) % ngroups;
+  int kblk, bg;
+  kv_block_of(static_cast<int>(blockIdx.x), ngroups, (p.Tk + KBM - 1) / KBM, kblk, bg);
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int kb = kblk * KBM;
   const int qt0 = max(kb - p.delta, 0) / P2, qt1 = (p.T - 1) / P2;
@@ -1040,8 +1060,8 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
   uint64_t* s_full = q_empty + C::NSTAGE;
   uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;
-  uint64_t* drain_g = p_full + 1;
-  uint64_t* drain = p_full + 2;
+  uint64_t* drain_g = p_full + 1;  // [2]: one per gradient-product issuer
+  uint64_t* drain = p_full + 3;
   uint64_t* last_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -1052,14 +1072,15 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
     mbar_init(kv_full, 1);
     for (int i = 0; i < C::NSTAGE; ++i) {
       mbar_init(&q_full[i], 1 + 32);  // TMA arrive + one cp.async arrival per producer lane
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 2);      // the dV and the dK issuer
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);  // one arrival per gradient warp
     mbar_init(p_full, 8);
     mbar_init(drain, 1);
-    mbar_init(drain_g, 1);
-    mbar_init(last_done, 1);
+    mbar_init(&drain_g[0], 1);
+    mbar_init(&drain_g[1], 1);
+    mbar_init(last_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1165,39 +1186,37 @@ __global__ void __launch_bounds__(Dkv64Cfg::THREADS, 1)
         mbar_wait(drain, 0, &never);
       }
     }
-  } else if (warp == 10) {
-    // ---------------------------------------------------------------- dV, dK issuer
+  } else if (warp == 10 || warp == 11) {
+    // ---------------------------------------------------------------- dV (warp 10), dK (warp 11) issuers
     // dV, dK of tile j follow p_full(j), which the gradient warps signal only after reading
-    // S^T(j), dP^T(j): those MMAs have completed, so this thread's commit after dV, dK of
-    // tile j is the last use of the Q/dO stage and of P^T, dS^T.
+    // S^T(j), dP^T(j): those MMAs have completed, so each thread's commit after its product
+    // of tile j is its last use of the Q/dO stage and of P^T (dS^T); q_empty completes when
+    // both have committed.
     if (lane == 0) {
+      const int w = warp - 10;  // 0: dV += P^T dO, 1: dK += dS^T Q
       constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
       const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, K2N * 128, 1024);  // MN-major Q/dO tiles
+      const uint32_t d_tm = tmem + (w == 0 ? C::TM_DV : C::TM_DK);
+      const uint32_t a_tm = tmem + (w == 0 ? C::TM_P : C::TM_DS);
+      const uint32_t b_off = w == 0 ? C::QT_BYTES : 0;  // dO (for dV) or Q (for dK)
       bool ok = true;
       for (int j = 0; ok && j < n_q; ++j) {
-        // dV += P^T(j) dO_j, dK += dS^T(j) Q_j
         const int st = j % C::NSTAGE;
         ok = mbar_wait(p_full, j & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
-        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
+        const uint64_t b_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES + b_off);
 #pragma unroll
         for (int kk = 0; kk < K2N / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < K2N / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DS + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&q_empty[st]);  // also tells the gradient warps that P^T(j), dS^T(j) are read
+          mma_bf16_ts(d_tm, a_tm + kk * 8, sdesc_add(b_desc, kk * 16 * 128), IDESC_G, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&q_empty[st]);  // also tells the gradient warps that P^T(j) (dS^T(j)) is read
       }
       if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
-        mma_commit(drain_g);
+        mma_commit(&drain_g[w]);
         volatile int never = 0;
-        mbar_wait(drain_g, 0, &never);
+        mbar_wait(&drain_g[w], 0, &never);
       }
     }
   } else {
