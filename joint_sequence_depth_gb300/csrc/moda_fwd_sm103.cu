@@ -319,9 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (!C::SPLIT && warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (d = 128)
-    // One thread for both tiles: PV_0(i), S_0(i+1), PV_1(i), S_1(i+1) in this order, since
-    // S of the next key tile overwrites P of this one.
-    if (lane == 0) {
+    // One warp for both tiles (its elected lane issues): PV_0(i), S_0(i+1), PV_1(i), S_1(i+1)
+    // in this order, since S of the next key tile overwrites P of this one.
+    {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
       const uint64_t q_desc0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
@@ -332,19 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
         const int g = item / C::NSLOT;  // load generation of the slot
-        return mbar_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
+        return warp_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
       };
-      auto release = [&](int item) { mma_commit(&kv_empty[item % C::NSLOT]); };
+      auto release = [&](int item) { mma_commit_warp(&kv_empty[item % C::NSLOT]); };
       static_assert((C::NSLOT & (C::NSLOT - 1)) == 0, "ring size");
       auto issue_s = [&](int t, int item) {
         const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
         const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
         const uint32_t d_tmem = tmem + C::tm_s(t);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(d_tmem, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                      sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
-        mma_commit(&s_full[t]);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(d_tmem, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                        sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
+          mma_commit(&s_full[t]);
+        }
+        __syncwarp();
       };
       // pv_done is committed only after a tile's last PV of the unit (for its epilogue):
       // before that, S of the next key tile, issued after this PV, tells the softmax warps
@@ -352,22 +355,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int t, int item, bool acc, bool last) {
         const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
         const uint32_t p_tmem = tmem + C::tm_p(t);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + C::tm_o(t), p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
-                      (acc || kk > 0) ? 1u : 0u);
-        if (last) mma_commit(&pv_done[t]);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(tmem + C::tm_o(t), p_tmem + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
+                        (acc || kk > 0) ? 1u : 0u);
+          if (last) mma_commit(&pv_done[t]);
+        }
+        __syncwarp();
       };
-      // The issuing thread is on the critical path between MMA groups: item indices are
-      // kept incremental, and the depth and sequence steps have a loop each.
+      // The issuing warp is on the critical path between MMA groups: item indices are kept
+      // incremental, and the depth and sequence steps have a loop each.
       for (int k = 0; ok && k < n_c; ++k) {
         const Unit u = unit_at(p, cta, k);
         const int nA = u.ns[0], nB = u.ns[1];
         const bool two = nB > 0;
         const int sbase = base + u.nd_items;  // first sequence item
-        ok = mbar_wait(&q_full[0], k & 1, abort_flag) && mbar_wait(&q_full[1], k & 1, abort_flag);
+        ok = warp_wait(&q_full[0], k & 1, abort_flag) && warp_wait(&q_full[1], k & 1, abort_flag);
         if (!ok) break;
-        if (!two) mma_commit(&q_empty[1]);  // tile 1 unused in this unit
+        if (!two) mma_commit_warp(&q_empty[1]);  // tile 1 unused in this unit
         // S of step 0
         {
           const int ka = p.n_d > 0 ? base : sbase;
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           issue_s(0, ka);
-          if (nA == 1) mma_commit(&q_empty[0]);
+          if (nA == 1) mma_commit_warp(&q_empty[0]);
           if (two) {
             if (kb != ka && !wait_item(kb)) {
               ok = false;
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             issue_s(1, kb);
-            if (nB == 1) mma_commit(&q_empty[1]);
+            if (nB == 1) mma_commit_warp(&q_empty[1]);
             if (kb != ka) release(kb);
           }
           release(ka);
@@ -398,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool last = i + 1 == p.n_d;
           const int ka = last ? sbase : base + stride * (i + 1);
           const int kb = last ? sbase : ka + 1;
-          if (!wait_item(va) || !mbar_wait(&p_full[0], pcnt0 & 1, abort_flag) ||
-              (i == 0 && k > 0 && !mbar_wait(&o_free[0], (k - 1) & 1, abort_flag))) {
+          if (!wait_item(va) || !warp_wait(&p_full[0], pcnt0 & 1, abort_flag) ||
+              (i == 0 && k > 0 && !warp_wait(&o_free[0], (k - 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -412,10 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           issue_s(0, ka);
-          if (i + 2 == nA) mma_commit(&q_empty[0]);
+          if (i + 2 == nA) mma_commit_warp(&q_empty[0]);
           if (two) {
-            if (!wait_item(vb) || !mbar_wait(&p_full[1], pcnt1 & 1, abort_flag) ||
-                (i == 0 && k > 0 && !mbar_wait(&o_free[1], (k - 1) & 1, abort_flag))) {
+            if (!wait_item(vb) || !warp_wait(&p_full[1], pcnt1 & 1, abort_flag) ||
+                (i == 0 && k > 0 && !warp_wait(&o_free[1], (k - 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             issue_s(1, kb);
-            if (i + 2 == nB) mma_commit(&q_empty[1]);
+            if (i + 2 == nB) mma_commit_warp(&q_empty[1]);
             if (kb != ka) release(kb);
           }
           release(ka);
@@ -447,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (j < mA) {
-            if (!mbar_wait(&p_full[0], pcnt0 & 1, abort_flag) ||
-                (first && k > 0 && !mbar_wait(&o_free[0], (k - 1) & 1, abort_flag))) {
+            if (!warp_wait(&p_full[0], pcnt0 & 1, abort_flag) ||
+                (first && k > 0 && !warp_wait(&o_free[0], (k - 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
@@ -464,11 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (j + 1 < mA) {
             issue_s(0, ik);
-            if (j + 2 == mA) mma_commit(&q_empty[0]);
+            if (j + 2 == mA) mma_commit_warp(&q_empty[0]);
           }
           if (j < mB) {
-            if (!mbar_wait(&p_full[1], pcnt1 & 1, abort_flag) ||
-                (first && k > 0 && !mbar_wait(&o_free[1], (k - 1) & 1, abort_flag))) {
+            if (!warp_wait(&p_full[1], pcnt1 & 1, abort_flag) ||
+                (first && k > 0 && !warp_wait(&o_free[1], (k - 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           release(iv);  // V_j: every PV reading it is issued
           if (j + 1 < mB) {
             issue_s(1, ik);
-            if (j + 2 == mB) mma_commit(&q_empty[1]);
+            if (j + 2 == mB) mma_commit_warp(&q_empty[1]);
           }
           if (next) release(ik);  // K_{j+1}: every S reading it is issued
         }
@@ -488,17 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         raise_abort(abort_flag, p.status);
         // wait for every MMA already issued before TMEM is released
-        mma_commit(&drain[0]);
+        mma_commit_warp(&drain[0]);
         volatile int never = 0;
         mbar_wait(&drain[0], 0, &never);
       }
     }
   } else if (C::SPLIT && (warp == 1 || warp == 2)) {
     // ---------------------------------------------------------------- MMA issuers (d = 64)
-    // One thread per query tile t (warps 1 and 2), so neither tile's S/PV chain waits on
-    // the other's softmax.  Every K/V item is released twice: once by each tile that uses
-    // it, twice by its only user otherwise.
-    if (lane == 0) {
+    // One warp per query tile t (warps 1 and 2; the elected lane issues), so neither tile's
+    // S/PV chain waits on the other's softmax.  Every K/V item is released twice: once by
+    // each tile that uses it, twice by its only user otherwise.
+    {
       const int t = warp - 1;
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
@@ -512,27 +518,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
         const int g = item / C::NSLOT;  // load generation of the slot
-        return mbar_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
+        return warp_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
       };
       auto release = [&](int item, bool shared) {
-        mma_commit(&kv_empty[item % C::NSLOT]);
-        if (!shared) mma_commit(&kv_empty[item % C::NSLOT]);
+        if (elect_one()) {
+          mma_commit(&kv_empty[item % C::NSLOT]);
+          if (!shared) mma_commit(&kv_empty[item % C::NSLOT]);
+        }
+        __syncwarp();
       };
       auto issue_s = [&](int item) {
         const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(s_tm, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                      sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
-        mma_commit(&s_full[t]);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(s_tm, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                        sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
+          mma_commit(&s_full[t]);
+        }
+        __syncwarp();
         ++scnt;
       };
       auto issue_pv = [&](int item, bool acc) {
         const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(o_tm, p_tm + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O, (acc || kk > 0) ? 1u : 0u);
-        mma_commit(&pv_done[t]);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_bf16_ts(o_tm, p_tm + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+          mma_commit(&pv_done[t]);
+        }
+        __syncwarp();
       };
       for (int k = 0; ok && k < n_c; ++k) {
         const Unit u = unit_at(p, cta, k);
@@ -551,22 +566,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           vi = ki + 1;
           return i - p.n_d < nt_other;
         };
-        ok = mbar_wait(&q_full[t], k & 1, abort_flag);
+        ok = warp_wait(&q_full[t], k & 1, abort_flag);
         if (!ok) break;
         if (n_t == 0) {
-          mma_commit(&q_empty[t]);  // tile unused in this unit
+          mma_commit_warp(&q_empty[t]);  // tile unused in this unit
         } else {
           // S of step 0
           int ki, vi;
           bool sh = kv(0, ki, vi);
           if constexpr (C::SPLIT) {
-            if (scnt > 0 && !mbar_wait(&s_free[t], (scnt - 1) & 1, abort_flag)) ok = false;
+            if (scnt > 0 && !warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag)) ok = false;
           }
           if (ok && !wait_item(ki)) ok = false;
           if (ok) {
             tc_fence_after();
             issue_s(ki);
-            if (n_t == 1) mma_commit(&q_empty[t]);
+            if (n_t == 1) mma_commit_warp(&q_empty[t]);
             release(ki, sh);
           }
           for (int i = 0; ok && i < n_t; ++i) {
@@ -577,19 +592,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::SPLIT) {
               // S of step i+1 as soon as the softmax has read S of step i
               if (more) {
-                if (!mbar_wait(&s_free[t], (scnt - 1) & 1, abort_flag) || !wait_item(kn)) {
+                if (!warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag) || !wait_item(kn)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
                 issue_s(kn);
-                if (i + 2 == n_t) mma_commit(&q_empty[t]);
+                if (i + 2 == n_t) mma_commit_warp(&q_empty[t]);
                 release(kn, sh_n);
               }
             }
             // PV of step i once P is written
-            if (!wait_item(vi) || !mbar_wait(&p_full[t], pcnt & 1, abort_flag) ||
-                (i == 0 && k > 0 && !mbar_wait(&o_free[t], (k - 1) & 1, abort_flag))) {
+            if (!wait_item(vi) || !warp_wait(&p_full[t], pcnt & 1, abort_flag) ||
+                (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
@@ -607,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 issue_s(kn);
-                if (i + 2 == n_t) mma_commit(&q_empty[t]);
+                if (i + 2 == n_t) mma_commit_warp(&q_empty[t]);
                 release(kn, sh_n);
               }
             }
@@ -618,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         raise_abort(abort_flag, p.status);
         // wait for every MMA this thread issued before TMEM is released
-        mma_commit(&drain[t]);
+        mma_commit_warp(&drain[t]);
         volatile int never = 0;
         mbar_wait(&drain[t], 0, &never);
       }

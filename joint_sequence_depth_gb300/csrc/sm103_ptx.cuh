@@ -141,10 +141,30 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// One lane of a converged warp (the lowest active lane, the same one at every call when the
+// whole warp is active).  MMA-issuing roles run their loops warp-wide and issue each group
+// of tcgen05 instructions from the elected lane: a loop that runs in one lane alone issues
+// its MMAs markedly slower while softmax warps keep the SM sub-partition busy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrives on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// mma_commit from the elected lane of a converged warp (the lane that issued its MMAs).
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+  if (elect_one()) mma_commit(bar);
+  __syncwarp();
 }
 
 // 32 lanes x 32 consecutive 32-bit columns (this warp's lane quarter), then wait.
