@@ -39,20 +39,30 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA: the two Q tiles of each unit, then the K/V items of the unit in the
-//               order the MMA warp consumes them, into a ring of smem slots.
-//   warp 1      TMEM allocator and MMA issuer (one thread).  Per step i:
+//               order the MMA warps consume them, into a ring of smem slots.
+//   warp 1      TMEM allocator.  d = 128: the MMA-issuing warp for both tiles.  Per step i:
 //                 PV_0(i), S_0(i+1), PV_1(i), S_1(i+1)  with  S_t = Q_t K^T into TMEM
 //                 S[t] and O_t += P_t V (P_t read from TMEM), so the tensor core works on
 //                 one tile while the other tile's softmax runs.
+//   warps 1, 2  d = 64: one MMA-issuing warp per query tile; S_t of the next key tile is
+//               issued as soon as the softmax warps have read S_t (P_t has columns of its
+//               own), so S and the softmax overlap within a tile as well.
+//               The issuing warps run their loops warp-wide (every lane takes the waits
+//               and the decisions) and one elected lane issues each MMA group: a loop run
+//               by lane 0 alone issues markedly slower while softmax warps keep the SM
+//               sub-partition busy (measured on GB300: 79-89 against 64 cycles per
+//               128x128x16 MMA).
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: thread r owns row r
 //               (TMEM lane r), S read whole (128 columns); exp2 with a log2(e)-folded
-//               scale; P rounded to bf16 into the TMEM columns of S; O rescaled only when the running max of a row that
-//               already holds probability mass grows by more than 2^8 (exact: the final
-//               division uses the same stale max); a warp none of whose positions a depth
-//               tile covers writes P = 0 without reading S.  Then the epilogue o = O / l.
+//               scale; P rounded to bf16 (d = 128: into the TMEM columns of S); O rescaled
+//               only when the running max of a row that already holds probability mass
+//               grows by more than 2^8 (exact: the final division uses the same stale
+//               max); a warp none of whose positions a depth tile covers writes P = 0
+//               without reading S.  Then the epilogue o = O / l.
 //
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d); P is
-// packed bf16 in the first 64 columns of S_t.
+// TMEM columns, d = 128: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P is
+// packed bf16 in the first 64 columns of S_t.  d = 64: per tile t, S_t [256t, 256t+128),
+// P_t [256t+128, 256t+192), O_t [256t+192, 256t+256).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
