@@ -726,8 +726,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           // S read whole (d = 64: then handed back to the MMA issuer for the next key tile;
           // d = 128: P is written over it once every column is in registers)
+          // the load also returns the row's maximum over the 128 columns, which is the row
+          // max whenever no column of the row is masked
           uint32_t s[BN];
-          tmem_ld128(s_tmem, s);
+          float m_raw;
+          tmem_ld128_max(s_tmem, s, m_raw);
           if constexpr (C::SPLIT) {
             tc_fence_before();
             __syncwarp();
@@ -737,16 +740,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < BN; ++c)
               if (c < lo || c >= hi) s[c] = __float_as_uint(-INFINITY);
-          }
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < BN; c += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+            for (int c = 0; c < BN; c += 8) {
+              mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
+              mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+              mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+              mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+            }
+            m_raw = fmax3(mx0, mx1, fmaxf(mx2, mx3));
           }
-          const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+          const float m_tile = m_raw * sl2;
           // P_t is free once the previous PV of this tile completed (d = 128: S of this step,
           // issued after that PV, is complete, so it has)
           bool pv_waited = j == 0 || !C::SPLIT;
