@@ -631,6 +631,178 @@ def run_write(args, shape):
     return 0
 
 
+CP_METRIC = ("MoDA context-parallel fwd/bwd TFLOP/s (every rank's chunk pairs run in turn on one GPU) "
+             "and fraction of roofline, 1\u00d7GB300")
+# workload -> (problem, ranks simulated, chunk layout)
+CP_WORKLOADS = {"bf16_cp2_train": ("bf16_train", 2, "zigzag"), "bf16_cp4_train": ("bf16_train", 4, "zigzag")}
+
+
+def run_cp(args, name):
+    """Context-parallel pieces on one GPU: one step runs, rank after rank, every chunk pair
+    of the ring schedule through moda_fwd_partial / moda_merge_partial / moda_bwd_partial /
+    moda_convert_f32 (the exchange is a change of references, no kernel waits on another
+    rank).  value = the whole problem's FLOPs / step time, comparable with the unchunked
+    step.  Also timed alone: one fully visible chunk pair's partial forward (tensor-bound)
+    and one merge (HBM-bound)."""
+    base_name, ranks, layout = CP_WORKLOADS[name]
+    from joint_sequence_depth_gb300.inputs import WORKLOADS
+
+    base = WORKLOADS[base_name]
+    world, rank, local = dist_setup(args)
+    cfg = {"workload": f"{name}: {base_name} (B={base.B} H={base.H} Hkv={base.Hkv} T={base.T} d={base.d} "
+                       f"S={base.S} {base.dtype_name}) split over {ranks} ranks ({layout} chunks), "
+                       f"every rank's pairs on this GPU, forward+backward",
+           "global_batch": base.B, "seq_len": base.T, "depth_slots": base.S, "cp_ranks": ranks,
+           "l2": "inputs larger than L2 (no flush)"}
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps, warm = max(1, args.steps), max(0, args.warmup)
+        time_oracle_steps(base, 1024, warm) if warm else None
+        r = time_oracle_steps(base, 1024, steps)
+        line = {"impl": "reference", "metric": CP_METRIC, "value": r["value"], "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": steps, "warmup": warm, "ms_per_step": r["seconds_per_step"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": r["value"], "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    import torch.distributed as dist
+
+    from joint_sequence_depth_gb300 import binding
+    from joint_sequence_depth_gb300 import build as mbuild
+    from joint_sequence_depth_gb300 import context_parallel as cp
+    from joint_sequence_depth_gb300.inputs import make_inputs
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mbuild.build()
+    binding.load_library()
+    x = make_inputs(base, seed=rank_seed(base_name, rank), device=dev, with_dout=True)
+    names = ("q", "k", "v", "kd", "vd", "dout")
+    owned = cp.chunks_of(base.T, ranks, layout)
+    loc = {n: [[x[n].narrow(2, c.start, c.length).contiguous() for c in owned[r]] for r in range(ranks)]
+           for n in names}
+    kern = cp.LibraryKernels()
+    stream = torch.cuda.current_stream()
+
+    def step(inp):
+        o, lse = cp.simulate_ring_forward(inp["q"], inp["k"], inp["v"], inp["kd"], inp["vd"], base.T, ranks,
+                                          layout, kernels=kern)
+        grads = cp.simulate_ring_backward(inp["q"], inp["k"], inp["v"], inp["kd"], inp["vd"], o, lse, inp["dout"],
+                                          base.T, ranks, layout, kernels=kern)
+        return o, lse, grads
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(max(3, args.warmup)):
+        step(loc)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = binding.moda_launch_count()
+    e0.record(stream)
+    for _ in range(K):
+        step(loc)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = binding.moda_launch_count() - launches0
+    clk = clocks.stop()
+    if binding.moda_device_status() != 0:
+        raise RuntimeError("device status set after the timed steps")
+    ms_step = e0.elapsed_time(e1) / K
+    # one fully visible chunk pair (query chunk ranks..., key chunk 0) and one merge, alone
+    c_q, c_k = owned[ranks - 1][0], owned[0][0]
+    qq = loc["q"][ranks - 1][0]
+    kk, vv = loc["k"][0][0], loc["v"][0][0]
+    delta = c_q.start - c_k.start
+    o_p, l_p = binding.moda_fwd_partial(qq, kk, vv, None, None, delta)
+    o_acc = torch.empty(qq.shape, dtype=torch.float32, device=dev)
+    l_acc = torch.empty(qq.shape[:3], dtype=torch.float32, device=dev)
+    binding.moda_merge_partial(o_acc, l_acc, o_p, l_p, first=True)
+    reps = 20
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    tp, tm = [], []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.moda_fwd_partial(qq, kk, vv, None, None, delta, o=o_p, lse=l_p)
+        b.record(stream)
+        flush.zero_()
+        c, d_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(stream)
+        binding.moda_merge_partial(o_acc, l_acc, o_p, l_p)
+        d_.record(stream)
+        torch.cuda.synchronize()
+        tp.append(a.elapsed_time(b))
+        tm.append(c.elapsed_time(d_))
+    del flush
+    ms_pair, ms_merge = statistics.median(tp), statistics.median(tm)
+    peaks, peak_kind = load_peaks()
+    pair_flops = 4.0 * base.B * base.H * base.d * c_q.length * c_k.length
+    e = 2
+    rows = base.B * base.H * c_q.length
+    merge_bytes = rows * base.d * (4 + 4 + e) + rows * 4 * 3
+    roof = {"bound": "tensor", "achieved": pair_flops / (ms_pair * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": None, "kernel": "moda_fwd_tc_kernel (one fully visible chunk pair, no depth slots)",
+                 "peak_source": f"{peak_kind} (bf16 burst, cuBLAS)", "ms": ms_pair,
+                 "algorithmic": {"flops": pair_flops, "bytes": None}})
+    merge = {"bound": "hbm", "achieved": merge_bytes / (ms_merge * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s", "ms": ms_merge, "bytes": merge_bytes}
+    merge["frac"] = merge["achieved"] / merge["peak"]
+    # end to end: the inputs from pinned host memory into the chunks, every output back
+    host = {n: [[t.cpu().pin_memory() for t in per] for per in loc[n]] for n in names}
+    E = max(3, args.e2e_steps)
+
+    def e2e_step():
+        for n in names:
+            for r in range(ranks):
+                for t_dev, t_host in zip(loc[n][r], host[n][r]):
+                    t_dev.copy_(t_host, non_blocking=True)
+        o, lse, grads = step(loc)
+        outs = [t for per in o for t in per] + [t for per in lse for t in per]
+        for g in grads:
+            outs += [t for per in g for t in per if t is not None]
+        return [t.to("cpu", non_blocking=True) for t in outs]
+
+    e2e_step()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(E):
+        back = e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / E
+    h2d = sum(t.numel() * t.element_size() for n in names for per in host[n] for t in per)
+    d2h = sum(t.numel() * t.element_size() for t in back)
+    ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev)
+    fl = flops(base)
+    total = fl["fwd"] + fl["bwd"]
+    if rank == 0:
+        line = {"metric": CP_METRIC, "value": aggregate_tflops(total, ms_step, world), "unit": "TFLOP/s",
+                "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": base.dtype_name,
+                "data": "synthetic", "config": cfg, "clocks": clk,
+                "e2e": {"value": aggregate_tflops(total, e2e_ms, world), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": launches, "roofline": roof, "merge": merge, "cpu_baseline": None}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def kernel_roofline(count, ms, peaks):
     """Roofline of one kernel launch: its algorithmic FLOPs against the burst bf16 peak or
     its algorithmic bytes against the copy bandwidth, whichever takes longer."""
@@ -713,6 +885,8 @@ def main():
         return run_decode(args, DECODE_WORKLOADS[args.workload])
     if args.workload in WRITE_WORKLOADS:
         return run_write(args, WRITE_WORKLOADS[args.workload])
+    if args.workload in CP_WORKLOADS:
+        return run_cp(args, args.workload)
     base = WORKLOADS[args.workload]
     shape = base
     if args.impl == "reference":
