@@ -33,6 +33,8 @@ RING = [
     ("d128_g8_w2_zigzag", 1, 16, 2, 390, 128, 2, bf16, 2, "zigzag"),
     ("d64_g2_no_depth_w3", 1, 4, 2, 700, 64, 0, bf16, 3, "contiguous"),
     ("fp32_d64_w2", 1, 4, 2, 300, 64, 3, f32, 2, "zigzag"),
+    # G = 16: the bf16 backward of every pair runs on the CUDA cores (float32 accumulators)
+    ("d64_g16_w2_cuda_core_bwd", 1, 16, 1, 300, 64, 2, bf16, 2, "contiguous"),
 ]
 
 
@@ -234,3 +236,41 @@ def test_convert_rounds_like_round_to_nearest_even(n):
     torch.cuda.synchronize()
     assert torch.equal(out.cpu(), src.cpu().to(bf16))
     assert torch.equal(out32, src)
+
+
+def test_ring_schedule_with_a_half_full_slot_ring():
+    """A bounded slot buffer (capacity 8, 3 slots read, NaN in the unread ones) through the
+    chunked path: the depth fold of each chunk reads only its first 3 slots."""
+    B, H, Hkv, T, d, S, C = 1, 8, 2, 500, 64, 3, 8
+    shape = Shape("cp_ring", B, H, Hkv, T, d, S, bf16, backward=True, slot_capacity=C)
+    x = make_inputs(shape, seed=77)
+    for n in ("kd", "vd"):
+        x[n][:, :, :, S:] = float("nan")
+    dev = torch.device("cuda:0")
+    g = {n: x[n].to(dev) for n in NAMES}
+    world, layout = 3, "contiguous"
+    owned = cp.chunks_of(T, world, layout)
+    loc = {n: [_split(g[n], owned[r]) for r in range(world)] for n in NAMES}
+    kern = cp.LibraryKernels(slots=S)
+    o, lse = cp.simulate_ring_forward(loc["q"], loc["k"], loc["v"], loc["kd"], loc["vd"], T, world, layout,
+                                      kernels=kern)
+    grads = cp.simulate_ring_backward(loc["q"], loc["k"], loc["v"], loc["kd"], loc["vd"], o, lse, loc["dout"], T,
+                                      world, layout, kernels=kern)
+    torch.cuda.synchronize()
+    chunks = [c for cs in owned for c in cs]
+    flat = lambda per_rank: [p for r in range(world) for p in per_rank[r]]  # noqa: E731
+    hx = {n: host_view(x[n]) for n in NAMES}
+    hx["kd"] = np.ascontiguousarray(hx["kd"][:, :, :, :S])
+    hx["vd"] = np.ascontiguousarray(hx["vd"][:, :, :, :S])
+    args = [hx[n] for n in NAMES]
+    ro, rl = oracle.forward(*args[:5])
+    assert max_abs(as_f64(_assemble(flat(o), chunks, T)), ro) < TOL_OUT[bf16]
+    assert max_abs(as_f64(_assemble(flat(lse), chunks, T)), rl) < TOL_OUT[bf16]
+    ref = oracle.backward(*args)
+    for i, nm in enumerate(("dq", "dk", "dv")):
+        got = as_f64(_assemble(flat(grads[i]), chunks, T))
+        assert rel_err(got, ref[i]) < TOL_GRAD_REL, (nm, rel_err(got, ref[i]))
+    for i, nm in ((3, "dkd"), (4, "dvd")):
+        got = as_f64(_assemble(flat(grads[i]), chunks, T))
+        assert np.all(got[:, :, :, S:] == 0), nm  # unread slots get zero gradient
+        assert rel_err(got[:, :, :, :S], ref[i]) < TOL_GRAD_REL, (nm, rel_err(got[:, :, :, :S], ref[i]))
