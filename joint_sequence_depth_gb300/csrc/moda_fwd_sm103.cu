@@ -261,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0, issued = 0, q_issued0 = 0, q_issued1 = 0;
       bool ok = true;
+      // Q tiles and depth slabs are read once: evict first, so they do not displace the
+      // sequence K/V that other query tiles read again
+      const uint64_t pol_once = l2_policy_evict_first();
       for (int k = 0; ok && k < n_c; ++k) {
         const Unit u = unit_at(p, cta, k);
         for (int t = 0; ok && t < 2; ++t) {
@@ -272,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&q_full[t], (D / 64) * p.G * p.P * 128);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(dst + h * (BM * 128), &tmQ, &q_full[t], h * 64, u.g * p.G, u.p0 + t * p.P, u.b);
+            tma_load_4d_hint(dst + h * (BM * 128), &tmQ, &q_full[t], h * 64, u.g * p.G, u.p0 + t * p.P, u.b,
+                             pol_once);
           if (t == 0)
             q_issued0 = k + 1;
           else
@@ -299,12 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int row = (u.bg * p.T + u.p0 + t * p.P) * p.S + i * BN;
               mbar_arrive_expect_tx(full, C::TILE_BYTES);
 #pragma unroll
-              for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * (BN * 128), map, full, h * 64, row);
+              for (int h = 0; h < D / 64; ++h)
+                tma_load_2d_hint(dst + h * (BN * 128), map, full, h * 64, row, pol_once);
             } else {
               const int pos0 = u.bg * p.T + u.p0 + t * p.P + i * p.dpt;
               mbar_arrive_expect_tx(full, static_cast<uint32_t>(D) * p.S_read * p.dpt * 2);
 #pragma unroll
-              for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * (BN * 128), map, full, h * 64, 0, pos0);
+              for (int h = 0; h < D / 64; ++h)
+                tma_load_3d_hint(dst + h * (BN * 128), map, full, h * 64, 0, pos0, pol_once);
             }
           } else {
             mbar_arrive_expect_tx(full, C::TILE_BYTES);
