@@ -71,6 +71,7 @@ struct BwdTcParams {
   float* dq_accum;  // depth share of dq, float32 [B,H,T,d] (read by the dQ kernel when S > 0)
   __nv_bfloat16 *dq, *dk, *dv, *dkd, *dvd;
   float *dq_acc, *dk_acc, *dv_acc;  // set: dq/dk/dv are added to these in float32 instead
+  int n_cta;  // CTAs of the persistent dQ kernel (d = 64)
   int* status;
 };
 
@@ -1381,6 +1382,33 @@ struct Dq64Cfg {
   static constexpr uint32_t TM_COLS = 512;
 };
 
+// Row blocks of the persistent dQ kernel: block index i -> (position block, b, kv head), the
+// longest rows first; CTA c takes blocks c, 2C-1-c, 2C+c, ... (snake order over C CTAs), so
+// that every CTA gets a similar amount of work.
+__device__ __forceinline__ int dq_blocks_of_cta(int n_blocks, int n_cta, int c) {
+  const int R = n_blocks / n_cta, rem = n_blocks % n_cta;
+  const bool extra = (R & 1) ? (n_cta - 1 - c < rem) : (c < rem);
+  return R + (extra ? 1 : 0);
+}
+
+struct DqBlock {
+  int b, g, bg, p0, n_kv;
+};
+
+__device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int c, int k) {
+  const int idx = k * p.n_cta + ((k & 1) ? p.n_cta - 1 - c : c);
+  const int ngroups = p.B * p.Hkv;
+  const int n_pb = (p.T + P - 1) / P;
+  DqBlock x;
+  x.bg = idx % ngroups;
+  x.b = x.bg / p.Hkv;
+  x.g = x.bg % p.Hkv;
+  x.p0 = (n_pb - 1 - idx / ngroups) * P;
+  const int p_last = min(x.p0 + P, p.T) - 1;
+  x.n_kv = min((p_last + p.delta) / Q2N + 1, (p.Tk + Q2N - 1) / Q2N);
+  return x;
+}
+
 __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     moda_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const BwdTcParams p) {
@@ -1394,14 +1422,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = QBM / p.G;
-  const int n_pb = (p.T + P - 1) / P;
-  const int ngroups = p.B * p.Hkv;
-  const int pb = n_pb - 1 - static_cast<int>(blockIdx.x) / ngroups;  // longest rows first
-  const int bg = static_cast<int>(blockIdx.x) % ngroups;
-  const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int p0 = pb * P;
-  const int p_last = min(p0 + P, p.T) - 1;
-  const int n_kv = min((p_last + p.delta) / Q2N + 1, (p.Tk + Q2N - 1) / Q2N);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int n_blk = dq_blocks_of_cta((p.T + P - 1) / P * p.B * p.Hkv, p.n_cta, cta);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
@@ -1448,26 +1470,32 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases and ring slots follow the running count of key tiles over the CTA's
+  // blocks (it), q_full and last_done the block count (k).
   if (warp == 0) {
     // ---------------------------------------------------------------- K_j, V_j loads
+    // (the loads of the next block start while this block's last tiles are processed)
     if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j % C::NSLOT, use = j / C::NSLOT;
-        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
-          raise_abort(abort_flag, p.status);
-          break;
+      int it = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const DqBlock x = dq_block_at(p, P, cta, k);
+        for (int j = 0; j < x.n_kv; ++j, ++it) {
+          const int slot = it % C::NSLOT, use = it / C::NSLOT;
+          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
+            raise_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
+          mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+          tma_load_3d(dst, &tmK, &kv_full[slot], 0, j * Q2N, x.bg);
+          tma_load_3d(dst + C::KV_BYTES, &tmV, &kv_full[slot], 0, j * Q2N, x.bg);
         }
-        uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
-        mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
-        tma_load_3d(dst, &tmK, &kv_full[slot], 0, j * Q2N, bg);
-        tma_load_3d(dst + C::KV_BYTES, &tmV, &kv_full[slot], 0, j * Q2N, bg);
-        issued = j + 1;
       }
       if (*abort_flag) {
         volatile int never = 0;
-        for (int j = max(0, issued - C::NSLOT); j < issued; ++j)
-          mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
+        for (int j = max(0, it - C::NSLOT); j < it; ++j) mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
       }
     }
   } else if (warp == 1) {
@@ -1475,28 +1503,33 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, Q2N, false);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);  // K-major
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        // S(j) = Q K_j^T once K_j, V_j are loaded and the gradient warps have read S of
-        // tile j-1; dP(j) = dO V_j^T once they have read dP of tile j-1
-        const int slot = j % C::NSLOT;
-        ok = mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag) &&
-             (j == 0 || mbar_wait(s_free, (j - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
-        const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
+      bool ok = true;
+      int it = 0;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const int n_kv = dq_block_at(p, P, cta, k).n_kv;
+        ok = mbar_wait(q_full, k & 1, abort_flag);  // Q and dO of this block in TMEM
+        for (int j = 0; ok && j < n_kv; ++j, ++it) {
+          // S = Q K_j^T once K_j, V_j are loaded and the gradient warps have read the
+          // previous S; dP = dO V_j^T once they have read the previous dP
+          const int slot = it % C::NSLOT;
+          ok = mbar_wait(&kv_full[slot], (it / C::NSLOT) & 1, abort_flag) &&
+               (it == 0 || mbar_wait(s_free, (it - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
+          const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_S, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
-        mma_commit(s_full);
-        ok = j == 0 || mbar_wait(dp_free, (j - 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_S, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, kk * 32), IDESC_S, kk > 0);
+          mma_commit(s_full);
+          ok = it == 0 || mbar_wait(dp_free, (it - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DP, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
-        mma_commit(dp_full);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DP, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, kk * 32), IDESC_S, kk > 0);
+          mma_commit(dp_full);
+        }
       }
       if (!ok) {
         raise_abort(abort_flag, p.status);
@@ -1509,25 +1542,31 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     // ---------------------------------------------------------------- dQ issuer
     // dQ(j) is issued after ds_full(j), which the gradient warps signal only after reading
     // S(j), dP(j): those MMAs have completed, so this thread's commit after dQ(j) is the
-    // last use of K_j, V_j and frees their slot.
+    // last use of K_j, V_j and frees their slot.  The first dQ of a block overwrites the
+    // accumulator: the gradient warps signal its ds_full only after their epilogue of the
+    // previous block has read it.
     if (lane == 0) {
       constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, Q2N * 128, 1024);  // MN-major
       bool ok = true;
-      for (int jj = 0; ok && jj < n_kv; ++jj) {
-        const int slot = jj % C::NSLOT;
-        ok = mbar_wait(ds_full, jj & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
-        const uint32_t ds = C::TM_DS + (jj & 1) * 64;
+      int it = 0;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const int n_kv = dq_block_at(p, P, cta, k).n_kv;
+        for (int j = 0; j < n_kv; ++j, ++it) {
+          const int slot = it % C::NSLOT;
+          ok = mbar_wait(ds_full, it & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
+          const uint32_t ds = C::TM_DS + (it & 1) * 64;
 #pragma unroll
-        for (int kk = 0; kk < Q2N / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&kv_empty[slot]);  // K_jj, V_jj and dS(jj) no longer read
+          for (int kk = 0; kk < Q2N / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DQ, tmem + ds + kk * 8, sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&kv_empty[slot]);  // K_j, V_j and dS(j) no longer read
+        }
+        if (ok) mma_commit(last_done);  // this block's dQ is complete
       }
-      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain_dq);
@@ -1540,13 +1579,15 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     const int wg = (warp - 2) >> 2;
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int pos = p0 + r / p.G;
-    const bool valid = (r < P * p.G) && pos < p.T;
-    const int h = g * p.G + r % p.G;
-    const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
-    if (wg == 0) {
-      // row r of Q and dO into TMEM lane r (the A operands of S and dP): column c holds
-      // elements 2c, 2c+1, i.e. the row's 32-bit words as stored
+    const bool row_in = r < P * p.G;
+    const float sl2 = p.scale_log2;
+    // row r of Q and dO of block k into TMEM lane r (the A operands of S and dP): column c
+    // holds elements 2c, 2c+1, i.e. the row's 32-bit words as stored
+    auto load_q = [&](int k) {
+      const DqBlock x = dq_block_at(p, P, cta, k);
+      const int pos = x.p0 + r / p.G;
+      const bool valid = row_in && pos < p.T;
+      const int64_t row = (static_cast<int64_t>(x.b) * p.H + x.g * p.G + r % p.G) * p.T + (valid ? pos : 0);
       const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
       const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
       uint32_t qw[32], ow[32];
@@ -1568,125 +1609,133 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_full);
-    }
-    const float2 stt = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
-    const float nlse2 = stt.x;  // -lse * log2(e)
-    const float dlt = stt.y;
-    const float sl2 = p.scale_log2;
-    const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
+    };
+    if (wg == 0 && n_blk > 0) load_q(0);
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = warp_wait(s_full, j & 1, abort_flag);
-      if (!ok) break;
-      tc_fence_after();
-      // P from S first, while dP may still be computed; then dS = P (dP - Delta)
-      float e[64];
-      {
-        uint32_t s[64];
-        tmem_ld64(tmem + lane_base + C::TM_S + wg * 64, s);
+    int it = 0;
+    for (int k = 0; ok && k < n_blk; ++k) {
+      const DqBlock x = dq_block_at(p, P, cta, k);
+      const int pos = x.p0 + r / p.G;
+      const bool valid = row_in && pos < p.T;
+      const int h = x.g * p.G + r % p.G;
+      const int64_t row = (static_cast<int64_t>(x.b) * p.H + h) * p.T + (valid ? pos : 0);
+      const float2 stt = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
+      const float nlse2 = stt.x;  // -lse * log2(e)
+      const float dlt = stt.y;
+      const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
+      for (int j = 0; j < x.n_kv; ++j, ++it) {
+        ok = warp_wait(s_full, it & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        // P from S first, while dP may still be computed; then dS = P (dP - Delta)
+        float e[64];
+        {
+          uint32_t s[64];
+          tmem_ld64(tmem + lane_base + C::TM_S + wg * 64, s);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
+            e[c] = ex2(e[c]);
+            e[c + 1] = ex2(e[c + 1]);
+          }
+          const int lim = valid ? key_end - (j * Q2N + wg * 64) : -1;  // columns c <= lim are visible
+          if (lim < 63) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+          }
+        }
+        ok = warp_wait(dp_full, it & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dpv[64];
+        tmem_ld64(tmem + lane_base + C::TM_DP + wg * 64, dpv);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
+        if (lane == 0) mbar_arrive(dp_free);
+        const uint32_t ds = C::TM_DS + (it & 1) * 64 + wg * 32;
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
-          e[c] = ex2(e[c]);
-          e[c + 1] = ex2(e[c + 1]);
-        }
-        const int lim = valid ? key_end - (j * Q2N + wg * 64) : -1;  // columns c <= lim are visible
-        if (lim < 63) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+          for (int c = 0; c < 32; c += 2) {
+            float d0, d1;
+            fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dlt, dlt,
+                     e[hf * 32 + c], e[hf * 32 + c + 1], d0, d1);
+            pk[c >> 1] = pack_bf16(d0, d1);
+          }
+          // dS buffer (it & 1) was last read by the dQ product two tiles earlier (its commit
+          // completes that tile's phase of kv_empty)
+          if (hf == 0 && it >= 2) {
+            ok = warp_wait(&kv_empty[(it - 2) % C::NSLOT], ((it - 2) / C::NSLOT) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          tmem_st16_nowait(tmem + lane_base + ds + hf * 16, pk);
         }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
       }
-      ok = warp_wait(dp_full, j & 1, abort_flag);
+      if (!ok) break;
+      // the S and dP products of this block have completed (their results were read): Q and
+      // dO of the next block can replace theirs while this block's epilogue runs
+      if (wg == 0 && k + 1 < n_blk) load_q(k + 1);
+      ok = warp_wait(last_done, k & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld64(tmem + lane_base + C::TM_DP + wg * 64, dpv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dp_free);
-      const uint32_t ds = C::TM_DS + (j & 1) * 64 + wg * 32;
+      // warpgroup w writes dq columns [32w, 32w+32)
+      const int c0 = wg * 32;
+      uint32_t acc[32];
+      tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
+      float extra[32];
+      if (p.S > 0 && valid) {
+        const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float d0, d1;
-          fsubmul2(__uint_as_float(dpv[hf * 32 + c]), __uint_as_float(dpv[hf * 32 + c + 1]), dlt, dlt,
-                   e[hf * 32 + c], e[hf * 32 + c + 1], d0, d1);
-          pk[c >> 1] = pack_bf16(d0, d1);
+        for (int i = 0; i < 8; ++i) {
+          const float4 e4 = src[i];
+          extra[4 * i] = e4.x;
+          extra[4 * i + 1] = e4.y;
+          extra[4 * i + 2] = e4.z;
+          extra[4 * i + 3] = e4.w;
         }
-        // dS buffer (j & 1) was last read by the dQ product of tile j-2 (its commit
-        // completes tile j-2's phase of kv_empty)
-        if (hf == 0 && j >= 2) {
-          ok = warp_wait(&kv_empty[(j - 2) % C::NSLOT], ((j - 2) / C::NSLOT) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        tmem_st16_nowait(tmem + lane_base + ds + hf * 16, pk);
-      }
-      if (!ok) break;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
-    }
-    if (!ok) {
-      raise_abort(abort_flag, p.status);
-    } else {
-      ok = warp_wait(last_done, 0, abort_flag);
-      if (!ok) {
-        raise_abort(abort_flag, p.status);
       } else {
-        tc_fence_after();
-        // warpgroup w writes dq columns [32w, 32w+32)
-        const int c0 = wg * 32;
-        uint32_t acc[32];
-        tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
-        float extra[32];
-        if (p.S > 0 && valid) {
-          const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 e4 = src[i];
-            extra[4 * i] = e4.x;
-            extra[4 * i + 1] = e4.y;
-            extra[4 * i + 2] = e4.z;
-            extra[4 * i + 3] = e4.w;
-          }
-        } else {
+        for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+      }
+      if (valid && p.dq_acc != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+        for (int i = 0; i < 8; ++i) {
+          float4 y = dst[i];
+          y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
+          y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
+          y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
+          y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
+          dst[i] = y;
         }
-        if (valid && p.dq_acc != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 y = dst[i];
-            y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
-            y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
-            y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
-            y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
-            dst[i] = y;
+        for (int i = 0; i < 4; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const int c = 8 * i + 2 * k2;
+            w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
+                              fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
           }
-        } else if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const int c = 8 * i + 2 * k2;
-              w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
-                                fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
-            }
-            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      // the accumulator read is complete (tcgen05.ld waits) before this warp's next ds_full
+      tc_fence_before();
     }
+    if (!ok) raise_abort(abort_flag, p.status);
   }
   __syncwarp();
   tc_fence_before();
@@ -1699,6 +1748,13 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
 }
 
 // ============================================================================ host
+int bwd_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
 }
@@ -1798,7 +1854,10 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     moda_bwd_dkdv64_kernel<<<grid_kv, Dkv64Cfg::THREADS, Dkv64Cfg::SMEM, s>>>(tk128, tv128, tq2, to2, p);
     mark_event(a, 5, s);
     mark_event(a, 6, s);
-    moda_bwd_dq64_kernel<<<grid_q, Dq64Cfg::THREADS, Dq64Cfg::SMEM, s>>>(tk128, tv128, p);
+    const int sms = bwd_sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    p.n_cta = static_cast<int>(std::min<unsigned>(grid_q, static_cast<unsigned>(sms)));
+    moda_bwd_dq64_kernel<<<p.n_cta, Dq64Cfg::THREADS, Dq64Cfg::SMEM, s>>>(tk128, tv128, p);
     mark_event(a, 7, s);
   } else {
     // d = 128: 64-column tiles, double-buffered TMEM, two gradient warpgroups splitting
