@@ -1370,11 +1370,14 @@ struct Dq64Cfg {
   static constexpr int THREADS = 64 + 256 + 32;
   static constexpr int KV_BYTES = Q2N * D * 2;  // one K (or V) tile; a ring slot holds both
   static constexpr int NSLOT = 3;
-  static constexpr int OFF_KV = 0;  // Q and dO live in TMEM, not here
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, (spare), drain, last_done,
-  // dp_full, dp_free
-  static constexpr int NBAR = 2 * NSLOT + 10;
+  static constexpr int OFF_KV = 0;
+  // Q and dO of a block staged by TMA (128-byte swizzle) on their way into TMEM
+  static constexpr int QS_BYTES = QBM * D * 2;
+  static constexpr int OFF_QS = OFF_KV + NSLOT * 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_QS + 2 * QS_BYTES;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full, s_free, ds_full, drain_dq, qs_full, drain, last_done,
+  // dp_full, dp_free, qs_empty
+  static constexpr int NBAR = 2 * NSLOT + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   // Q and dO of the CTA's rows stay in TMEM (A operands of S and dP, bf16 pairs)
@@ -1411,6 +1414,7 @@ __device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int 
 
 __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     moda_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                          const BwdTcParams p) {
   using C = Dq64Cfg;
   constexpr int D = C::D;
@@ -1437,6 +1441,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   uint64_t* last_done = drain + 1;
   uint64_t* dp_full = last_done + 1;  // S and dP complete, and are released, separately
   uint64_t* dp_free = dp_full + 1;
+  uint64_t* qs_full = ds_full + 2;   // a block's Q and dO staged in shared memory
+  uint64_t* qs_empty = dp_free + 1;  // ... and copied from there into TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -1445,6 +1451,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
+    mbar_init(qs_full, 1);
+    mbar_init(qs_empty, 128);  // warpgroup 0 of the gradient warps
     mbar_init(q_full, 128);
     mbar_init(s_full, 1);
     mbar_init(s_free, 8);  // one arrival per gradient warp
@@ -1460,6 +1468,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TM_COLS);
@@ -1476,10 +1486,20 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     // ---------------------------------------------------------------- K_j, V_j loads
     // (the loads of the next block start while this block's last tiles are processed)
     if (lane == 0) {
-      int it = 0;
+      int it = 0, staged = 0;
       bool ok = true;
       for (int k = 0; ok && k < n_blk; ++k) {
         const DqBlock x = dq_block_at(p, P, cta, k);
+        // this block's Q and dO rows (position-major, positions past T read as zeros) into
+        // the staging buffer, once the previous block's have been copied out of it
+        if (k > 0 && !mbar_wait(qs_empty, (k - 1) & 1, abort_flag)) {
+          raise_abort(abort_flag, p.status);
+          break;
+        }
+        mbar_arrive_expect_tx(qs_full, 2u * p.G * P * 128u);
+        tma_load_4d(smem + C::OFF_QS, &tmQ, qs_full, 0, x.g * p.G, x.p0, x.b);
+        tma_load_4d(smem + C::OFF_QS + C::QS_BYTES, &tmO, qs_full, 0, x.g * p.G, x.p0, x.b);
+        staged = k + 1;
         for (int j = 0; j < x.n_kv; ++j, ++it) {
           const int slot = it % C::NSLOT, use = it / C::NSLOT;
           if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
@@ -1496,6 +1516,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       if (*abort_flag) {
         volatile int never = 0;
         for (int j = max(0, it - C::NSLOT); j < it; ++j) mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
+        if (staged > 0) mbar_wait(qs_full, (staged - 1) & 1, &never);
       }
     }
   } else if (warp == 1) {
@@ -1582,19 +1603,18 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     const bool row_in = r < P * p.G;
     const float sl2 = p.scale_log2;
     // row r of Q and dO of block k into TMEM lane r (the A operands of S and dP): column c
-    // holds elements 2c, 2c+1, i.e. the row's 32-bit words as stored
-    auto load_q = [&](int k) {
-      const DqBlock x = dq_block_at(p, P, cta, k);
-      const int pos = x.p0 + r / p.G;
-      const bool valid = row_in && pos < p.T;
-      const int64_t row = (static_cast<int64_t>(x.b) * p.H + x.g * p.G + r % p.G) * p.T + (valid ? pos : 0);
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + row * D);
-      const uint4* orow = reinterpret_cast<const uint4*>(p.dout + row * D);
+    // holds elements 2c, 2c+1, i.e. the row's 32-bit words as stored.  The rows come from
+    // the staging buffer (row r: 128 bytes, 16-byte chunk c at chunk c ^ (r % 8)); rows past
+    // P*G, which the TMA box does not cover, are zero.
+    auto load_q = [&](int k) -> bool {
+      if (!warp_wait(qs_full, k & 1, abort_flag)) return false;
+      const uint32_t qs = sbase + C::OFF_QS + r * 128;
       uint32_t qw[32], ow[32];
 #pragma unroll
       for (int ch = 0; ch < D / 8; ++ch) {
-        const uint4 a = valid ? __ldg(qrow + ch) : make_uint4(0, 0, 0, 0);
-        const uint4 o = valid ? __ldg(orow + ch) : make_uint4(0, 0, 0, 0);
+        const uint32_t off = static_cast<uint32_t>((ch ^ (r & 7)) << 4);
+        const uint4 a = row_in ? ld_shared_v4(qs + off) : make_uint4(0, 0, 0, 0);
+        const uint4 o = row_in ? ld_shared_v4(qs + C::QS_BYTES + off) : make_uint4(0, 0, 0, 0);
         qw[4 * ch] = a.x;
         qw[4 * ch + 1] = a.y;
         qw[4 * ch + 2] = a.z;
@@ -1604,22 +1624,37 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
         ow[4 * ch + 2] = o.z;
         ow[4 * ch + 3] = o.w;
       }
+      mbar_arrive(qs_empty);
       tmem_st32_nowait(tmem + lane_base + C::TM_Q, qw);
       tmem_st32_nowait(tmem + lane_base + C::TM_DO, ow);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_full);
+      return true;
     };
-    if (wg == 0 && n_blk > 0) load_q(0);
-    bool ok = true;
+    // global row of thread r in block k, and whether it exists
+    auto row_of = [&](int k, bool& valid) -> int64_t {
+      const DqBlock x = dq_block_at(p, P, cta, k);
+      const int pos = x.p0 + r / p.G;
+      valid = row_in && pos < p.T;
+      return (static_cast<int64_t>(x.b) * p.H + x.g * p.G + r % p.G) * p.T + (valid ? pos : 0);
+    };
+    bool ok = !(wg == 0 && n_blk > 0) || load_q(0);
     int it = 0;
+    // row statistics of the next block, loaded while this block runs
+    float2 stt_next = make_float2(-INFINITY, 0.f);
+    if (n_blk > 0) {
+      bool v0;
+      const int64_t r0 = row_of(0, v0);
+      if (v0) stt_next = p.stats[r0];
+    }
     for (int k = 0; ok && k < n_blk; ++k) {
       const DqBlock x = dq_block_at(p, P, cta, k);
       const int pos = x.p0 + r / p.G;
       const bool valid = row_in && pos < p.T;
       const int h = x.g * p.G + r % p.G;
       const int64_t row = (static_cast<int64_t>(x.b) * p.H + h) * p.T + (valid ? pos : 0);
-      const float2 stt = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
+      const float2 stt = stt_next;
       const float nlse2 = stt.x;  // -lse * log2(e)
       const float dlt = stt.y;
       const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
@@ -1683,15 +1718,15 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       }
       if (!ok) break;
       // the S and dP products of this block have completed (their results were read): Q and
-      // dO of the next block can replace theirs while this block's epilogue runs
-      if (wg == 0 && k + 1 < n_blk) load_q(k + 1);
-      ok = warp_wait(last_done, k & 1, abort_flag);
-      if (!ok) break;
-      tc_fence_after();
-      // warpgroup w writes dq columns [32w, 32w+32)
+      // dO of the next block replace theirs first, so that the next block's products can
+      // start while this block's epilogue runs
+      if (wg == 0 && k + 1 < n_blk && !load_q(k + 1)) {
+        ok = false;
+        break;
+      }
+      // warpgroup w writes dq columns [32w, 32w+32); the depth share of those columns and the
+      // next block's row statistics are loaded before the wait for the last dQ product
       const int c0 = wg * 32;
-      uint32_t acc[32];
-      tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
       float extra[32];
       if (p.S > 0 && valid) {
         const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
@@ -1707,6 +1742,16 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) extra[i] = 0.f;
       }
+      if (k + 1 < n_blk) {
+        bool vn;
+        const int64_t rn = row_of(k + 1, vn);
+        stt_next = vn ? p.stats[rn] : make_float2(-INFINITY, 0.f);
+      }
+      ok = warp_wait(last_done, k & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
       if (valid && p.dq_acc != nullptr) {
         float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
 #pragma unroll
@@ -1769,6 +1814,23 @@ bool make_map(CUtensorMap* map, const void* base, int D, int T, int planes, int 
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(depth)};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q (or dO) [B][H][T][D] bf16 described as (D, H, T, B) -- heads before positions -- so that a
+// box 64 x G x P x 1 lands position-major (row = position * G + head); positions past T read
+// as zeros.
+bool make_qpos_map(CUtensorMap* map, const void* base, int D, int T, int H, int B, int P, int G) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(T) * D * 2, static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * T * D * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(P), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1857,7 +1919,10 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     const int sms = bwd_sm_count();
     if (sms <= 0) return cudaErrorNoDevice;
     p.n_cta = static_cast<int>(std::min<unsigned>(grid_q, static_cast<unsigned>(sms)));
-    moda_bwd_dq64_kernel<<<p.n_cta, Dq64Cfg::THREADS, Dq64Cfg::SMEM, s>>>(tk128, tv128, p);
+    CUtensorMap tq4, to4;
+    if (!make_qpos_map(&tq4, a.q, D, pr.T, pr.H, pr.B, P, pr.G) || !make_qpos_map(&to4, a.dout, D, pr.T, pr.H, pr.B, P, pr.G))
+      return cudaErrorInvalidValue;
+    moda_bwd_dq64_kernel<<<p.n_cta, Dq64Cfg::THREADS, Dq64Cfg::SMEM, s>>>(tk128, tv128, tq4, to4, p);
     mark_event(a, 7, s);
   } else {
     // d = 128: 64-column tiles, double-buffered TMEM, two gradient warpgroups splitting
