@@ -1655,6 +1655,8 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       const int h = x.g * p.G + r % p.G;
       const int64_t row = (static_cast<int64_t>(x.b) * p.H + h) * p.T + (valid ? pos : 0);
       const float2 stt = stt_next;
+      // the depth share this thread adds in the epilogue (one 128-byte line) into L2 now
+      if (p.S > 0 && valid) prefetch_l2(p.dq_accum + row * D + wg * 32);
       const float nlse2 = stt.x;  // -lse * log2(e)
       const float dlt = stt.y;
       const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
