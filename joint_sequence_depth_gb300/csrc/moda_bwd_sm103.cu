@@ -328,10 +328,39 @@ __global__ void __launch_bounds__(256) moda_bwd_depth_kernel(const BwdTcParams p
   }
 }
 
+// Row blocks of the persistent dQ kernels: block index i -> (position block, b, kv head), the
+// longest rows first; CTA c takes blocks c, 2C-1-c, 2C+c, ... (snake order over C CTAs), so
+// that every CTA gets a similar amount of work.
+__device__ __forceinline__ int dq_blocks_of_cta(int n_blocks, int n_cta, int c) {
+  const int R = n_blocks / n_cta, rem = n_blocks % n_cta;
+  const bool extra = (R & 1) ? (n_cta - 1 - c < rem) : (c < rem);
+  return R + (extra ? 1 : 0);
+}
+
+struct DqBlock {
+  int b, g, bg, p0, n_kv;
+};
+
+__device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int c, int k, int tile_keys) {
+  const int idx = k * p.n_cta + ((k & 1) ? p.n_cta - 1 - c : c);
+  const int ngroups = p.B * p.Hkv;
+  const int n_pb = (p.T + P - 1) / P;
+  DqBlock x;
+  x.bg = idx % ngroups;
+  x.b = x.bg / p.Hkv;
+  x.g = x.bg % p.Hkv;
+  x.p0 = (n_pb - 1 - idx / ngroups) * P;
+  const int p_last = min(x.p0 + P, p.T) - 1;
+  x.n_kv = min((p_last + p.delta) / tile_keys + 1, (p.Tk + tile_keys - 1) / tile_keys);
+  return x;
+}
+
 // ============================================================================ dQ
-// CTA: 128 expanded rows of (b, g), position-major (row r -> position p0 + r/G,
-// head g*G + r%G), P = floor(128/G) positions.  Keys in tiles of 64.
-// Used at d = 128 (d = 64 has a kernel of its own below).
+// Persistent CTAs (one per SM) walking row blocks of 128 expanded rows of (b, g),
+// position-major (row r -> position p0 + r/G, head g*G + r%G), P = floor(128/G) positions.
+// Keys in tiles of 64.  Used at d = 128 (d = 64 has a kernel of its own below).  A block's
+// Q and dO are staged by TMA and copied into TMEM by warpgroup 0 right after the previous
+// block's last tile; the K/V ring runs on across blocks.
 // Warps: 0 TMA (K_j and V_j in one transaction), 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient
 // warps (warp w owns TMEM lanes 32*(w%4) ..; with two warpgroups WG k handles key
 // columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also writes the
@@ -347,10 +376,14 @@ struct DqCfg {
   static constexpr int THREADS = 64 + 128 * NWG;
   static constexpr int KV_BYTES = QBN * D * 2;  // one K (or V) tile; a ring slot holds both
   static constexpr int NSLOT = 4;
-  static constexpr int OFF_KV = 0;  // Q and dO live in TMEM
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * 2 * KV_BYTES;
-  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[NBUF], ds_full[NBUF], drain, last_done
-  static constexpr int NBAR = 2 * NSLOT + 3 + 2 * NBUF;
+  static constexpr int OFF_KV = 0;
+  // Q and dO of a block staged by TMA (64-column halves, 128-byte swizzle) on their way into TMEM
+  static constexpr int QS_HALF = QBM * 128;
+  static constexpr int OFF_QS = OFF_KV + NSLOT * 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_QS + 2 * (D / 64) * QS_HALF;
+  // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[NBUF], ds_full[NBUF], drain, last_done,
+  // qs_full, qs_empty
+  static constexpr int NBAR = 2 * NSLOT + 5 + 2 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   // Q and dO of the CTA's rows (bf16 pairs, D/2 columns each) are the A operands of S, dP
@@ -364,6 +397,7 @@ struct DqCfg {
 template <int D, int NBUF, int NWG>
 __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 1)
     moda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
                        const BwdTcParams p) {
   using C = DqCfg<D, NBUF, NWG>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -374,14 +408,8 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = QBM / p.G;
-  const int n_pb = (p.T + P - 1) / P;
-  const int ngroups = p.B * p.Hkv;
-  const int pb = n_pb - 1 - static_cast<int>(blockIdx.x) / ngroups;
-  const int bg = static_cast<int>(blockIdx.x) % ngroups;
-  const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int p0 = pb * P;
-  const int p_last = min(p0 + P, p.T) - 1;
-  const int n_kv = min((p_last + p.delta) / QBN + 1, (p.Tk + QBN - 1) / QBN);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int n_blk = dq_blocks_of_cta((p.T + P - 1) / P * p.B * p.Hkv, p.n_cta, cta);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
@@ -391,6 +419,8 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
   uint64_t* ds_full = s_full + NBUF;
   uint64_t* drain = ds_full + NBUF;
   uint64_t* last_done = drain + 1;
+  uint64_t* qs_full = last_done + 1;   // a block's Q and dO staged in shared memory
+  uint64_t* qs_empty = qs_full + 1;    // ... and copied from there into TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -406,12 +436,16 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
     }
     mbar_init(drain, 1);
     mbar_init(last_done, 1);
+    mbar_init(qs_full, 1);
+    mbar_init(qs_empty, 128);  // warpgroup 0 of the gradient warps
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TM_COLS);
@@ -422,43 +456,68 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases, ring slots and S/dP buffers follow the running count of key tiles over
+  // the CTA's row blocks; q_full, qs_full/qs_empty and last_done follow the block count.
   if (warp == 0) {
-    // ---------------------------------------------------------------- K_j, V_j loads
+    // ---------------------------------------------------------------- Q/dO staging, K_j, V_j loads
     if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j % C::NSLOT, use = j / C::NSLOT;
-        if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
+      int it = 0, staged = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const DqBlock x = dq_block_at(p, P, cta, k, QBN);
+        // this block's Q and dO rows (position-major; positions past T read as zeros), once
+        // the previous block's have been copied out of the staging buffer
+        if (k > 0 && !mbar_wait(qs_empty, (k - 1) & 1, abort_flag)) {
           raise_abort(abort_flag, p.status);
           break;
         }
-        uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
-        mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+        mbar_arrive_expect_tx(qs_full, 2u * (D / 64) * p.G * P * 128u);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(dst + h * (QBN * 128), &tmK, &kv_full[slot], h * 64, j * QBN, bg);
-          tma_load_3d(dst + C::KV_BYTES + h * (QBN * 128), &tmV, &kv_full[slot], h * 64, j * QBN, bg);
+          tma_load_4d(smem + C::OFF_QS + h * C::QS_HALF, &tmQ, qs_full, h * 64, x.g * p.G, x.p0, x.b);
+          tma_load_4d(smem + C::OFF_QS + (D / 64 + h) * C::QS_HALF, &tmO, qs_full, h * 64, x.g * p.G, x.p0, x.b);
         }
-        issued = j + 1;
+        staged = k + 1;
+        for (int j = 0; j < x.n_kv; ++j, ++it) {
+          const int slot = it % C::NSLOT, use = it / C::NSLOT;
+          if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
+            raise_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + C::OFF_KV + slot * 2 * C::KV_BYTES;
+          mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_3d(dst + h * (QBN * 128), &tmK, &kv_full[slot], h * 64, j * QBN, x.bg);
+            tma_load_3d(dst + C::KV_BYTES + h * (QBN * 128), &tmV, &kv_full[slot], h * 64, j * QBN, x.bg);
+          }
+        }
       }
       if (*abort_flag) {
         volatile int never = 0;
-        for (int j = max(0, issued - C::NSLOT); j < issued; ++j)
-          mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
+        for (int j = max(0, it - C::NSLOT); j < it; ++j) mbar_wait(&kv_full[j % C::NSLOT], (j / C::NSLOT) & 1, &never);
+        if (staged > 0) mbar_wait(qs_full, (staged - 1) & 1, &never);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // S/dP of tile t+NBUF follow dQ of tile t (S and dP of a buffer overwrite the dS that
+    // dQ reads); the S/dP lookahead runs into the next block once its Q and dO are in TMEM.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, QBN, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       // descriptors built once; each MMA only advances the start address
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
       const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, QBN * 128, 1024);    // MN-major
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      auto issue_s = [&](int j) -> bool {
-        const int slot = j % C::NSLOT, bf = j % NBUF;
-        if (!mbar_wait(&kv_full[slot], (j / C::NSLOT) & 1, abort_flag)) return false;
+      bool ok = true;
+      // S/dP cursor: block ks, tile js of it (n_ks tiles), global tile index ts
+      int ks = 0, js = 0, ts = 0;
+      int n_ks = n_blk > 0 ? dq_block_at(p, P, cta, 0, QBN).n_kv : 0;
+      auto issue_s = [&]() -> bool {
+        if (js == 0 && !mbar_wait(q_full, ks & 1, abort_flag)) return false;
+        const int slot = ts % C::NSLOT, bf = ts % NBUF;
+        if (!mbar_wait(&kv_full[slot], (ts / C::NSLOT) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
         const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
@@ -473,26 +532,34 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
           mma_bf16_ts(tmem + C::TM_DP + bf * QBN, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, boff), IDESC_S, kk > 0);
         }
         mma_commit(&s_full[bf]);
+        ++ts;
+        if (++js == n_ks) {
+          js = 0;
+          ++ks;
+          n_ks = ks < n_blk ? dq_block_at(p, P, cta, ks, QBN).n_kv : 0;
+        }
         return true;
       };
-      auto issue_dq = [&](int j) -> bool {
-        const int slot = j % C::NSLOT, bf = j % NBUF;
-        if (!mbar_wait(&ds_full[bf], (j / NBUF) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
+      auto s_left = [&]() { return ks < n_blk; };
+      for (int i = 0; ok && i < NBUF && s_left(); ++i) ok = issue_s();
+      int t = 0;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const int n_kv = dq_block_at(p, P, cta, k, QBN).n_kv;
+        for (int j = 0; ok && j < n_kv; ++j, ++t) {
+          const int slot = t % C::NSLOT, bf = t % NBUF;
+          ok = mbar_wait(&ds_full[bf], (t / NBUF) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < QBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + kk * 8, sdesc_add(k_desc, kk * 16 * 128),
-                      IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&kv_empty[slot]);  // K_j, V_j no longer read
-        return true;
-      };
-      for (int j = 0; ok && j < NBUF && j < n_kv; ++j) ok = issue_s(j);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        ok = issue_dq(j);
-        if (ok && j + NBUF < n_kv) ok = issue_s(j + NBUF);
+          for (int kk = 0; kk < QBN / 16; ++kk)
+            mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + kk * 8, sdesc_add(k_desc, kk * 16 * 128),
+                        IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&kv_empty[slot]);  // K_t, V_t no longer read
+          if (j + 1 == n_kv) mma_commit(last_done);  // this block's dQ is complete
+          if (s_left()) ok = issue_s();
+        }
       }
-      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
@@ -506,135 +573,169 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
     constexpr int NCOL = QBN / NWG;  // key columns of a tile this warpgroup forms
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int pos = p0 + r / p.G;
-    const bool valid = (r < P * p.G) && pos < p.T;
-    const int h = g * p.G + r % p.G;
-    const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + (valid ? pos : 0);
-    if (wg == 0) {
-      // row r of Q and dO into TMEM lane r, 32 columns (64 elements) at a time: column c
-      // holds elements 2c, 2c+1, the row's 32-bit words as stored
+    const bool row_in = r < P * p.G;
+    // row r of Q and dO of block k into TMEM lane r: column c holds elements 2c, 2c+1, the
+    // row's 32-bit words as stored.  The rows come from the staging buffer (per 64-column
+    // half, row r: 128 bytes, 16-byte chunk c at chunk c ^ (r % 8)); rows past P*G, which the
+    // TMA box does not cover, are zero.
+    auto load_q = [&](int k) -> bool {
+      if (!warp_wait(qs_full, k & 1, abort_flag)) return false;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
-        const uint4* src = reinterpret_cast<const uint4*>((part ? p.dout : p.q) + row * D);
-        const uint32_t dst = tmem + lane_base + (part ? C::TM_DO : C::TM_Q);
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        for (int h = 0; h < D / 64; ++h) {
+          const uint32_t src = sbase + C::OFF_QS + (part * (D / 64) + h) * C::QS_HALF + r * 128;
           uint32_t w[32];
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
-            const uint4 a = valid ? __ldg(src + c0 / 4 + ch) : make_uint4(0, 0, 0, 0);
+            const uint4 a = row_in ? ld_shared_v4(src + ((ch ^ (r & 7)) << 4)) : make_uint4(0, 0, 0, 0);
             w[4 * ch] = a.x;
             w[4 * ch + 1] = a.y;
             w[4 * ch + 2] = a.z;
             w[4 * ch + 3] = a.w;
           }
-          tmem_st32_nowait(dst + c0, w);
+          tmem_st32_nowait(tmem + lane_base + (part ? C::TM_DO : C::TM_Q) + h * 32, w);
         }
       }
+      mbar_arrive(qs_empty);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_full);
-    }
-    const float2 st = valid ? p.stats[row] : make_float2(-INFINITY, 0.f);
-    const float nlse2 = st.x;  // -lse * log2(e)
-    const float dlt = st.y;
+      return true;
+    };
+    auto row_of = [&](int k, bool& valid) -> int64_t {
+      const DqBlock x = dq_block_at(p, P, cta, k, QBN);
+      const int pos = x.p0 + r / p.G;
+      valid = row_in && pos < p.T;
+      return (static_cast<int64_t>(x.b) * p.H + x.g * p.G + r % p.G) * p.T + (valid ? pos : 0);
+    };
+    bool ok = !(wg == 0 && n_blk > 0) || load_q(0);
     const float sl2 = p.scale_log2;
-    const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int bf = j % NBUF;
-      ok = warp_wait(&s_full[bf], (j / NBUF) & 1, abort_flag);
+    float2 stt_next = make_float2(-INFINITY, 0.f);  // row statistics of the next block
+    if (n_blk > 0) {
+      bool v0;
+      const int64_t r0 = row_of(0, v0);
+      if (v0) stt_next = p.stats[r0];
+    }
+    int t = 0;
+    for (int k = 0; ok && k < n_blk; ++k) {
+      const DqBlock x = dq_block_at(p, P, cta, k, QBN);
+      const int pos = x.p0 + r / p.G;
+      const bool valid = row_in && pos < p.T;
+      const int h = x.g * p.G + r % p.G;
+      const int64_t row = (static_cast<int64_t>(x.b) * p.H + h) * p.T + (valid ? pos : 0);
+      const float nlse2 = stt_next.x;  // -lse * log2(e)
+      const float dlt = stt_next.y;
+      // the depth share this thread adds in the epilogue into L2 now
+      if (p.S > 0 && valid) {
+#pragma unroll
+        for (int c0 = wg * (D / NWG); c0 < (wg + 1) * (D / NWG); c0 += 32) prefetch_l2(p.dq_accum + row * D + c0);
+      }
+      const int key_end = min(pos + p.delta, p.Tk - 1);  // last key this row sees
+      for (int j = 0; j < x.n_kv; ++j, ++t) {
+        const int bf = t % NBUF;
+        ok = warp_wait(&s_full[bf], (t / NBUF) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pk[NCOL / 2];
+#pragma unroll
+        for (int hf = 0; hf < NCOL / 32; ++hf) {
+          const int c0 = wg * NCOL + hf * 32;  // first key column of this group
+          uint32_t s[32], dpv[32];
+          tmem_ld32x2(tmem + lane_base + C::TM_S + bf * QBN + c0, tmem + lane_base + C::TM_DP + bf * QBN + c0, s, dpv);
+          const int lim = valid ? key_end - (j * QBN + c0) : -1;  // columns c <= lim are visible
+          float e[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
+            e[c] = ex2(e[c]);
+            e[c + 1] = ex2(e[c + 1]);
+          }
+          if (lim < 31) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float d0, d1;
+            fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, dlt, e[c], e[c + 1], d0, d1);
+            pk[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
+          }
+        }
+        // dS (bf16 pairs) over the first 32 columns of S[bf]; this warpgroup's share
+        if constexpr (NCOL == 64)
+          tmem_st32(tmem + lane_base + C::TM_S + bf * QBN, pk);
+        else
+          tmem_st16(tmem + lane_base + C::TM_S + bf * QBN + wg * 16, pk);
+        tc_fence_before();
+        mbar_arrive(&ds_full[bf]);
+      }
+      if (!ok) break;
+      // the S and dP products of this block have completed (their results were read): Q and
+      // dO of the next block replace theirs first, so that the next block's products can
+      // start while this block's epilogue runs
+      if (wg == 0 && k + 1 < n_blk && !load_q(k + 1)) {
+        ok = false;
+        break;
+      }
+      if (k + 1 < n_blk) {
+        bool vn;
+        const int64_t rn = row_of(k + 1, vn);
+        stt_next = vn ? p.stats[rn] : make_float2(-INFINITY, 0.f);
+      }
+      ok = warp_wait(last_done, k & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      uint32_t pk[NCOL / 2];
-#pragma unroll
-      for (int hf = 0; hf < NCOL / 32; ++hf) {
-        const int c0 = wg * NCOL + hf * 32;  // first key column of this group
-        uint32_t s[32], dpv[32];
-        tmem_ld32x2(tmem + lane_base + C::TM_S + bf * QBN + c0, tmem + lane_base + C::TM_DP + bf * QBN + c0, s, dpv);
-        const int lim = valid ? key_end - (j * QBN + c0) : -1;  // columns c <= lim are visible
-        float e[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          ffma2(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, nlse2, nlse2, e[c], e[c + 1]);
-          e[c] = ex2(e[c]);
-          e[c + 1] = ex2(e[c + 1]);
-        }
-        if (lim < 31) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) e[c] = (c <= lim) ? e[c] : 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float d0, d1;
-          fsubmul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, dlt, e[c], e[c + 1], d0, d1);
-          pk[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
-        }
-      }
-      // dS (bf16 pairs) over the first 32 columns of S[bf]; this warpgroup's share
-      if constexpr (NCOL == 64)
-        tmem_st32(tmem + lane_base + C::TM_S + bf * QBN, pk);
-      else
-        tmem_st16(tmem + lane_base + C::TM_S + bf * QBN + wg * 16, pk);
-      tc_fence_before();
-      mbar_arrive(&ds_full[bf]);
-    }
-    if (!ok) {
-      raise_abort(abort_flag, p.status);
-    } else {
-      ok = warp_wait(last_done, 0, abort_flag);
-      if (!ok) {
-        raise_abort(abort_flag, p.status);
-      } else {
-        tc_fence_after();
-        // WG w writes dq columns [w*D/NWG, (w+1)*D/NWG)
+      // WG w writes dq columns [w*D/NWG, (w+1)*D/NWG)
 #pragma unroll 1
-        for (int c0 = wg * (D / NWG); c0 < (wg + 1) * (D / NWG); c0 += 32) {
-          uint32_t acc[32];
-          tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
-          float extra[32];
-          if (p.S > 0 && valid) {
-            const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
+      for (int c0 = wg * (D / NWG); c0 < (wg + 1) * (D / NWG); c0 += 32) {
+        uint32_t acc[32];
+        tmem_ld32(tmem + lane_base + C::TM_DQ + c0, acc);
+        float extra[32];
+        if (p.S > 0 && valid) {
+          const float4* src = reinterpret_cast<const float4*>(p.dq_accum + row * D + c0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 e = src[i];
-              extra[4 * i] = e.x;
-              extra[4 * i + 1] = e.y;
-              extra[4 * i + 2] = e.z;
-              extra[4 * i + 3] = e.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+          for (int i = 0; i < 8; ++i) {
+            const float4 e = src[i];
+            extra[4 * i] = e.x;
+            extra[4 * i + 1] = e.y;
+            extra[4 * i + 2] = e.z;
+            extra[4 * i + 3] = e.w;
           }
-          if (valid && p.dq_acc != nullptr) {
-            float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 y = dst[i];
-              y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
-              y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
-              y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
-              y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
-              dst[i] = y;
+          for (int i = 0; i < 32; ++i) extra[i] = 0.f;
+        }
+        if (valid && p.dq_acc != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(p.dq_acc + row * D + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 y = dst[i];
+            y.x += fmaf(__uint_as_float(acc[4 * i]), p.scale, extra[4 * i]);
+            y.y += fmaf(__uint_as_float(acc[4 * i + 1]), p.scale, extra[4 * i + 1]);
+            y.z += fmaf(__uint_as_float(acc[4 * i + 2]), p.scale, extra[4 * i + 2]);
+            y.w += fmaf(__uint_as_float(acc[4 * i + 3]), p.scale, extra[4 * i + 3]);
+            dst[i] = y;
+          }
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int c = 8 * i + 2 * k2;
+              w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
+                                fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
             }
-          } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.dq + row * D + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t w[4];
-#pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2) {
-                const int c = 8 * i + 2 * k2;
-                w[k2] = pack_bf16(fmaf(__uint_as_float(acc[c]), p.scale, extra[c]),
-                                  fmaf(__uint_as_float(acc[c + 1]), p.scale, extra[c + 1]));
-              }
-              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
+      // the accumulator read is complete (tcgen05.ld waits) before this warp's next ds_full
+      tc_fence_before();
     }
+    if (!ok) raise_abort(abort_flag, p.status);
   }
   __syncwarp();
   tc_fence_before();
@@ -1385,33 +1486,6 @@ struct Dq64Cfg {
   static constexpr uint32_t TM_COLS = 512;
 };
 
-// Row blocks of the persistent dQ kernel: block index i -> (position block, b, kv head), the
-// longest rows first; CTA c takes blocks c, 2C-1-c, 2C+c, ... (snake order over C CTAs), so
-// that every CTA gets a similar amount of work.
-__device__ __forceinline__ int dq_blocks_of_cta(int n_blocks, int n_cta, int c) {
-  const int R = n_blocks / n_cta, rem = n_blocks % n_cta;
-  const bool extra = (R & 1) ? (n_cta - 1 - c < rem) : (c < rem);
-  return R + (extra ? 1 : 0);
-}
-
-struct DqBlock {
-  int b, g, bg, p0, n_kv;
-};
-
-__device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int c, int k) {
-  const int idx = k * p.n_cta + ((k & 1) ? p.n_cta - 1 - c : c);
-  const int ngroups = p.B * p.Hkv;
-  const int n_pb = (p.T + P - 1) / P;
-  DqBlock x;
-  x.bg = idx % ngroups;
-  x.b = x.bg / p.Hkv;
-  x.g = x.bg % p.Hkv;
-  x.p0 = (n_pb - 1 - idx / ngroups) * P;
-  const int p_last = min(x.p0 + P, p.T) - 1;
-  x.n_kv = min((p_last + p.delta) / Q2N + 1, (p.Tk + Q2N - 1) / Q2N);
-  return x;
-}
-
 __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     moda_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
@@ -1489,7 +1563,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       int it = 0, staged = 0;
       bool ok = true;
       for (int k = 0; ok && k < n_blk; ++k) {
-        const DqBlock x = dq_block_at(p, P, cta, k);
+        const DqBlock x = dq_block_at(p, P, cta, k, Q2N);
         // this block's Q and dO rows (position-major, positions past T read as zeros) into
         // the staging buffer, once the previous block's have been copied out of it
         if (k > 0 && !mbar_wait(qs_empty, (k - 1) & 1, abort_flag)) {
@@ -1527,7 +1601,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       bool ok = true;
       int it = 0;
       for (int k = 0; ok && k < n_blk; ++k) {
-        const int n_kv = dq_block_at(p, P, cta, k).n_kv;
+        const int n_kv = dq_block_at(p, P, cta, k, Q2N).n_kv;
         ok = mbar_wait(q_full, k & 1, abort_flag);  // Q and dO of this block in TMEM
         for (int j = 0; ok && j < n_kv; ++j, ++it) {
           // S = Q K_j^T once K_j, V_j are loaded and the gradient warps have read the
@@ -1572,7 +1646,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       bool ok = true;
       int it = 0;
       for (int k = 0; ok && k < n_blk; ++k) {
-        const int n_kv = dq_block_at(p, P, cta, k).n_kv;
+        const int n_kv = dq_block_at(p, P, cta, k, Q2N).n_kv;
         for (int j = 0; j < n_kv; ++j, ++it) {
           const int slot = it % C::NSLOT;
           ok = mbar_wait(ds_full, it & 1, abort_flag);
@@ -1634,7 +1708,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
     };
     // global row of thread r in block k, and whether it exists
     auto row_of = [&](int k, bool& valid) -> int64_t {
-      const DqBlock x = dq_block_at(p, P, cta, k);
+      const DqBlock x = dq_block_at(p, P, cta, k, Q2N);
       const int pos = x.p0 + r / p.G;
       valid = row_in && pos < p.T;
       return (static_cast<int64_t>(x.b) * p.H + x.g * p.G + r % p.G) * p.T + (valid ? pos : 0);
@@ -1649,7 +1723,7 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
       if (v0) stt_next = p.stats[r0];
     }
     for (int k = 0; ok && k < n_blk; ++k) {
-      const DqBlock x = dq_block_at(p, P, cta, k);
+      const DqBlock x = dq_block_at(p, P, cta, k, Q2N);
       const int pos = x.p0 + r / p.G;
       const bool valid = row_in && pos < p.T;
       const int h = x.g * p.G + r % p.G;
@@ -1940,7 +2014,13 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
     moda_bwd_dkdv_kernel<D, 2, 2><<<grid_kv, KC::THREADS, KC::SMEM, s>>>(tk128, tv128, tq, to, p);
     mark_event(a, 5, s);
     mark_event(a, 6, s);
-    moda_bwd_dq_kernel<D, 2, 2><<<grid_q, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, p);
+    const int sms = bwd_sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    p.n_cta = static_cast<int>(std::min<unsigned>(grid_q, static_cast<unsigned>(sms)));
+    CUtensorMap tq4, to4;
+    if (!make_qpos_map(&tq4, a.q, D, pr.T, pr.H, pr.B, P, pr.G) || !make_qpos_map(&to4, a.dout, D, pr.T, pr.H, pr.B, P, pr.G))
+      return cudaErrorInvalidValue;
+    moda_bwd_dq_kernel<D, 2, 2><<<p.n_cta, QC::THREADS, QC::SMEM, s>>>(tk64, tv64, tq4, to4, p);
     mark_event(a, 7, s);
   }
   count_launches(2);
