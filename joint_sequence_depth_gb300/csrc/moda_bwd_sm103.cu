@@ -368,8 +368,19 @@ __device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int 
 // tile j+1 while tile j's dS is formed.
 // TMEM: S[b] cols [64b, 64b+64), dP[b] [64(NBUF+b), ...), dQ [128 NBUF, 128 NBUF + d),
 // then Q and dO (bf16 pairs, d/2 columns each: the A operands of S and dP).  dS (bf16)
-// is written over the first 32 columns of S[b].
+// is written over S[b]: warpgroup w packs its 32 keys into the first 16 columns of its own
+// half [32w, 32w+32) (packed_col below), so no warpgroup overwrites columns another still reads.
 constexpr int QBM = 128, QBN = 64;
+
+// TMEM column (from the start of a 64-column S or dP buffer) of the bf16 pairs of keys (or
+// queries) 16kk .. 16kk+15, the A operand of step kk of a 64-deep gradient product.  With two
+// warpgroups splitting a buffer's 64 columns, warpgroup w packs its 32 values into the first
+// 16 columns of its own half [32w, 32w+32): columns the other warpgroup still reads are never
+// written.
+template <int NWG>
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return NWG == 2 ? static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8) : static_cast<uint32_t>(kk * 8);
+}
 
 template <int D, int NBUF, int NWG>
 struct DqCfg {
@@ -553,8 +564,8 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
           const uint64_t k_desc = sdesc_add(kv_desc_mn, slot * 2 * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < QBN / 16; ++kk)
-            mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + kk * 8, sdesc_add(k_desc, kk * 16 * 128),
-                        IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + packed_col<NWG>(kk),
+                        sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&kv_empty[slot]);  // K_t, V_t no longer read
           if (j + 1 == n_kv) mma_commit(last_done);  // this block's dQ is complete
           if (s_left()) ok = issue_s();
@@ -662,11 +673,11 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
             pk[hf * 16 + (c >> 1)] = pack_bf16(d0, d1);
           }
         }
-        // dS (bf16 pairs) over the first 32 columns of S[bf]; this warpgroup's share
+        // dS (bf16 pairs) over this warpgroup's own S columns of S[bf] (see packed_col)
         if constexpr (NCOL == 64)
           tmem_st32(tmem + lane_base + C::TM_S + bf * QBN, pk);
         else
-          tmem_st16(tmem + lane_base + C::TM_S + bf * QBN + wg * 16, pk);
+          tmem_st16(tmem + lane_base + C::TM_S + bf * QBN + wg * 32, pk);
         tc_fence_before();
         mbar_arrive(&ds_full[bf]);
       }
@@ -754,7 +765,8 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
 // Warps: 0 loads, 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient warps (thread = key = TMEM
 // lane; with two warpgroups WG k handles query columns [32k, 32k+32), with one all 64).
 // TMEM: S^T[b] cols [64b, ..), dP^T[b] [64(NBUF+b), ..), dV [128 NBUF, +d), dK [+d, +2d).
-// P^T and dS^T (bf16) overwrite the first 32 columns of their buffers.
+// P^T and dS^T (bf16) are written over their buffers the same way as dS in the dQ kernel
+// (packed_col): warpgroup w's 32 query columns into the first 16 columns of its own half.
 constexpr int KBM = 128, KBN = 64;
 
 template <int D, int NBUF, int NWG>
@@ -945,12 +957,12 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
         const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
 #pragma unroll
         for (int kk = 0; kk < KBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + bf * KBN + kk * 8, sdesc_add(o_desc, kk * 16 * 128), IDESC_G,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + bf * KBN + packed_col<NWG>(kk), sdesc_add(o_desc, kk * 16 * 128),
+                      IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < KBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + bf * KBN + kk * 8, sdesc_add(q_desc, kk * 16 * 128), IDESC_G,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + bf * KBN + packed_col<NWG>(kk),
+                      sdesc_add(q_desc, kk * 16 * 128), IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&q_empty[st]);
         return true;
       };
@@ -1034,8 +1046,9 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       if constexpr (NCOL == 64) {
         tmem_st32x2(tmem + lane_base + C::TM_S + bf * KBN, tmem + lane_base + C::TM_DP + bf * KBN, pp, pd);
       } else {
-        tmem_st16(tmem + lane_base + C::TM_S + bf * KBN + wg * 16, pp);
-        tmem_st16(tmem + lane_base + C::TM_DP + bf * KBN + wg * 16, pd);
+        // over this warpgroup's own S^T / dP^T columns (see packed_col)
+        tmem_st16(tmem + lane_base + C::TM_S + bf * KBN + wg * 32, pp);
+        tmem_st16(tmem + lane_base + C::TM_DP + bf * KBN + wg * 32, pd);
       }
       tc_fence_before();
       mbar_arrive(&p_full[bf]);

@@ -34,6 +34,12 @@ SMALL = [
     ("bf16_d64_g3_ragged", 1, 6, 2, 300, 64, 5, bf16),
     ("bf16_d64_g8", 1, 16, 2, 260, 64, 3, bf16),
     ("bf16_d64_g1_ctas_gt_sms", 2, 16, 16, 700, 64, 4, bf16),
+    # more row blocks than SMs, so the persistent dQ CTAs take several blocks each (blocks of
+    # different lengths, the next block's Q/dO staged while one runs): d = 128 with G = 1 and
+    # G = 4, and d = 64 with G = 4
+    ("bf16_d128_g1_blocks_gt_sms", 2, 16, 16, 700, 128, 4, bf16),
+    ("bf16_d128_g4_blocks_gt_sms", 2, 16, 4, 1100, 128, 3, bf16),
+    ("bf16_d64_g4_blocks_gt_sms", 2, 16, 4, 1100, 64, 3, bf16),
 ]
 
 
