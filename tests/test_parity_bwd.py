@@ -1,7 +1,7 @@
 """GPU backward parity: libmoda's moda_bwd (through the C ABI) against the float64 oracle.
 
 Small cases: every gradient element compared (relative max error per tensor).
-The full-size training workload: sampled positions (dq of the G heads, dkd, dvd)
+The full-size workloads: sampled positions (dq of the G heads, dkd, dvd)
 and sampled sequence keys (dk, dv), which the oracle computes one by one.
 """
 import zlib
@@ -67,9 +67,11 @@ def test_backward_small_elementwise(case):
         assert rel_err(gg, r) < TOL_GRAD_REL, (nm, rel_err(gg, r))
 
 
-def test_backward_full_size_sampled():
-    shape = WORKLOADS["bf16_train"]
-    x = make_inputs(shape, seed=SEEDS["bf16_train"], device="cuda", with_dout=True)
+@pytest.mark.parametrize("name", ["bf16_train", "bf16_mha", "bf16_gqa"])
+def test_backward_full_size_sampled(name):
+    # the d = 64 kernels (bf16_train) and the d = 128 ones (bf16_mha: G = 1, bf16_gqa: G = 4)
+    shape = WORKLOADS[name]
+    x = make_inputs(shape, seed=SEEDS[name], device="cuda", with_dout=True)
     o, lse = binding.moda_fwd(x["q"], x["k"], x["v"], x["kd"], x["vd"])
     dq, dk, dv, dkd, dvd = binding.moda_bwd(x["q"], x["k"], x["v"], x["kd"], x["vd"], o, lse, x["dout"])
     torch.cuda.synchronize()
