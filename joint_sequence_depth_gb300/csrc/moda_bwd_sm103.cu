@@ -1751,6 +1751,9 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
         ok = warp_wait(s_full, it & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
+        // the dS buffer (it & 1) is free once the dQ product two tiles earlier has read it (its
+        // commit completes that tile's phase of kv_empty): tested now, waited for only if not
+        const bool ds_free = it < 2 || mbar_test_wait(&kv_empty[(it - 2) % C::NSLOT], ((it - 2) / C::NSLOT) & 1);
         // P from S first, while dP may still be computed; then dS = P (dP - Delta)
         float e[64];
         {
@@ -1790,11 +1793,11 @@ __global__ void __launch_bounds__(Dq64Cfg::THREADS, 1)
                      e[hf * 32 + c], e[hf * 32 + c + 1], d0, d1);
             pk[c >> 1] = pack_bf16(d0, d1);
           }
-          // dS buffer (it & 1) was last read by the dQ product two tiles earlier (its commit
-          // completes that tile's phase of kv_empty)
           if (hf == 0 && it >= 2) {
-            ok = warp_wait(&kv_empty[(it - 2) % C::NSLOT], ((it - 2) / C::NSLOT) & 1, abort_flag);
-            if (!ok) break;
+            if (!__all_sync(0xffffffffu, ds_free)) {
+              ok = warp_wait(&kv_empty[(it - 2) % C::NSLOT], ((it - 2) / C::NSLOT) & 1, abort_flag);
+              if (!ok) break;
+            }
             tc_fence_after();
           }
           tmem_st16_nowait(tmem + lane_base + ds + hf * 16, pk);
