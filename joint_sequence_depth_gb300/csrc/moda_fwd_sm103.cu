@@ -679,9 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = pfirst + pl;
       const bool valid = n_t > 0 && pl < p.P && pos < p.T;
       float m_run = -INFINITY, l_run = 0.f;
+      bool s_ready = false;  // d = 64: S of this step found complete during the previous one
       for (int j = 0; j < n_t; ++j) {
-        ok = warp_wait(&s_full[t], scnt & 1, abort_flag);
-        if (!ok) break;
+        if (!s_ready) {
+          ok = warp_wait(&s_full[t], scnt & 1, abort_flag);
+          if (!ok) break;
+        }
+        s_ready = false;
         ++scnt;
         tc_fence_after();
         const bool depth = j < p.n_d;
@@ -791,8 +795,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P of the whole tile into registers first: only its store has to wait for the
           // previous PV of this tile to have read P_t
           uint32_t pk[BN / 2];
+          bool pv_ready = false, s_next = false;
 #pragma unroll
           for (int c = 0; c < BN; c += 4) {
+            if constexpr (C::SPLIT) {
+              if (c == BN / 2) {
+                // halfway through the exponentials, test (without waiting) whether the previous
+                // PV has read P_t and whether S of the next key tile, issued when this one was
+                // read, is complete: their latencies overlap the second half
+                if (!pv_waited) pv_ready = mbar_test_wait(&pv_done[t], (jcnt - 1) & 1);
+                if (j + 1 < n_t) s_next = mbar_test_wait(&s_full[t], scnt & 1);
+              }
+            }
             float x0, x1, x2, x3;
             ffma2_bc(__uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, -m_use, x0, x1);
             ffma2_bc(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]), sl2, -m_use, x2, x3);
@@ -808,11 +822,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[(c >> 1) + 1] = pack_bf16(x2, x3);
           }
           if (!pv_waited) {
-            ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
-            if (!ok) break;
+            if (!__all_sync(0xffffffffu, pv_ready)) {
+              ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
+              if (!ok) break;
+            }
             tc_fence_after();
           }
           tmem_st64(p_tmem, pk);
+          if constexpr (C::SPLIT) s_ready = __all_sync(0xffffffffu, s_next);
         }
         if (!ok) break;
         l_run += (ls0 + ls1) + (ls2 + ls3);
