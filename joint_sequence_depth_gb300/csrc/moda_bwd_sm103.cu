@@ -8,13 +8,14 @@
 //   depth kernel (CUDA cores, warp per position):  dvd = sum_h P^d dO,
 //       dkd = scale sum_h dS^d q, and the depth share of dq (scale sum_i dS^d kd_i),
 //       kept in float32 in the workspace.
-//   dK/dV kernel (tcgen05, one CTA per 128 keys of a kv head, looping over 64-row
-//       query tiles of the G heads):  S^T = K Q^T, dP^T = V dO^T into TMEM;
-//       thread k (TMEM lane k) forms P^T and dS^T, written back to TMEM as bf16;
-//       dV += P^T dO, dK += dS^T Q with A read from TMEM.
-//   dQ kernel (tcgen05, one CTA per 128 expanded query rows, looping over 64-key
-//       tiles):  S = Q K^T, dP = dO V^T; thread r forms dS (bf16 into TMEM);
-//       dQ += dS K.  The epilogue adds the depth share and rounds to bf16.
+//   dK/dV kernel (tcgen05, one CTA per 128 keys of a kv head, looping over query tiles
+//       of the G heads, 64 rows at d = 128, 128 at d = 64):  S^T = K Q^T, dP^T = V dO^T
+//       into TMEM; thread k (TMEM lane k) forms P^T and dS^T, written back to TMEM as
+//       bf16; dV += P^T dO, dK += dS^T Q with A read from TMEM.
+//   dQ kernel (tcgen05, persistent: one CTA per SM walking blocks of 128 expanded query
+//       rows, looping over key tiles of 64 at d = 128, 128 at d = 64):  S = Q K^T,
+//       dP = dO V^T; thread r forms dS (bf16 into TMEM); dQ += dS K.  The epilogue adds
+//       the depth share and rounds to bf16.
 //
 // All waits are bounded (see sm103_ptx.cuh); a timeout records MODA_ERR_TIMEOUT.
 #include <cudaTypedefs.h>
