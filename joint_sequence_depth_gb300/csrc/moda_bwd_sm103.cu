@@ -763,8 +763,11 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
 // CTA: 128 keys [kb, kb+128) of (b, g).  Query tiles of 64 rows, head-major inside the
 // tile (row r -> head g*G + r/P', position p0 + r%P', P' = floor(64/G)), loaded by TMA
 // together with dO; their LSE and Delta are copied asynchronously by the producer warp.
-// Warps: 0 loads, 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient warps (thread = key = TMEM
-// lane; with two warpgroups WG k handles query columns [32k, 32k+32), with one all 64).
+// Warps: 0 loads, 1 TMEM and the S^T/dP^T products, 2 .. 2+4*NWG-1 gradient warps
+// (thread = key = TMEM lane; with two warpgroups WG k handles query columns [32k, 32k+32),
+// with one all 64), 2+4*NWG the dV and 3+4*NWG the dK products: three issuing threads, so
+// that one waiting on a barrier leaves the others' MMAs running, and the N = 64 products
+// are not issued by one thread alone.
 // TMEM: S^T[b] cols [64b, ..), dP^T[b] [64(NBUF+b), ..), dV [128 NBUF, +d), dK [+d, +2d).
 // P^T and dS^T (bf16) are written over their buffers the same way as dS in the dQ kernel
 // (packed_col): warpgroup w's 32 query columns into the first 16 columns of its own half.
@@ -772,7 +775,7 @@ constexpr int KBM = 128, KBN = 64;
 
 template <int D, int NBUF, int NWG>
 struct DkvCfg {
-  static constexpr int THREADS = 64 + 128 * NWG;
+  static constexpr int THREADS = 64 + 128 * NWG + 64;  // + the dV and dK issuing warps
   static constexpr int KV_BYTES = KBM * D * 2;   // the CTA's K (or V) tile
   static constexpr int QT_BYTES = KBN * D * 2;   // one 64-row Q (or dO) tile
   static constexpr int NSTAGE = 4;
@@ -783,8 +786,8 @@ struct DkvCfg {
   static constexpr int OFF_STAT = OFF_Q + NSTAGE * STAGE_BYTES;  // [NSTAGE][64] {-lse*log2e, Delta}
   static constexpr int OFF_BAR = OFF_STAT + NSTAGE * 2 * KBN * 4;
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[NBUF], p_full[NBUF], drain, last_done,
-  // dp_full[NBUF] (S^T and dP^T of a buffer complete separately)
-  static constexpr int NBAR = 3 + 2 * NSTAGE + 3 * NBUF;
+  // dp_full[NBUF] (S^T and dP^T of a buffer complete separately), drain_g[2]
+  static constexpr int NBAR = 5 + 2 * NSTAGE + 3 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t TM_S = 0, TM_DP = 64 * NBUF, TM_DV = 128 * NBUF, TM_DK = 128 * NBUF + D;
@@ -824,6 +827,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
   uint64_t* drain = p_full + NBUF;
   uint64_t* last_done = drain + 1;
   uint64_t* dp_full = last_done + 1;
+  uint64_t* drain_g = dp_full + NBUF;  // [2]: the dV and the dK issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const float4* stat = reinterpret_cast<const float4*>(smem + C::OFF_STAT);  // two rows per float4
@@ -832,7 +836,7 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
     mbar_init(kv_full, 1);
     for (int i = 0; i < C::NSTAGE; ++i) {
       mbar_init(&q_full[i], 1 + 32);  // TMA arrive + one cp.async arrival per producer lane
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 2);  // the dV and the dK issuer
     }
     for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
@@ -840,7 +844,9 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
       mbar_init(&p_full[i], 128 * NWG);
     }
     mbar_init(drain, 1);
-    mbar_init(last_done, 1);
+    mbar_init(&drain_g[0], 1);
+    mbar_init(&drain_g[1], 1);
+    mbar_init(last_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -918,19 +924,21 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
         mbar_wait(&q_full[i % C::NSTAGE], (i / C::NSTAGE) & 1, &never);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S^T, dP^T issuer
+    // S^T and dP^T of tile i go to buffer i % NBUF, over the P^T and dS^T of tile i - NBUF:
+    // issued once the dV and dK products of that tile have completed (they commit q_empty)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(KBM, KBN, false);
-      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
       // descriptors built once; each MMA only advances the start address
       const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
       const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       const uint64_t qt_desc_k = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);           // K-major Q/dO tiles
-      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, KBN * 128, 1024);   // MN-major Q/dO tiles
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      auto issue_s = [&](int i) -> bool {
+      for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % C::NSTAGE, bf = i % NBUF;
-        if (!mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag)) return false;
+        ok = mbar_wait(&q_full[st], (i / C::NSTAGE) & 1, abort_flag) &&
+             (i < NBUF || mbar_wait(&q_empty[(i - NBUF) % C::NSTAGE], ((i - NBUF) / C::NSTAGE) & 1, abort_flag));
+        if (!ok) break;
         tc_fence_after();
         const uint64_t q_desc = sdesc_add(qt_desc_k, st * C::STAGE_BYTES);
         const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
@@ -948,36 +956,45 @@ __global__ void __launch_bounds__(DkvCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 :
           mma_bf16_ss(tmem + C::TM_DP + bf * KBN, sdesc_add(v_desc, aoff), sdesc_add(o_desc, boff), IDESC_S, kk > 0);
         }
         mma_commit(&dp_full[bf]);
-        return true;
-      };
-      auto issue_g = [&](int i) -> bool {
-        const int st = i % C::NSTAGE, bf = i % NBUF;
-        if (!mbar_wait(&p_full[bf], (i / NBUF) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t q_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES);
-        const uint64_t o_desc = sdesc_add(q_desc, C::QT_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < KBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + bf * KBN + packed_col<NWG>(kk), sdesc_add(o_desc, kk * 16 * 128),
-                      IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < KBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + bf * KBN + packed_col<NWG>(kk),
-                      sdesc_add(q_desc, kk * 16 * 128), IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&q_empty[st]);
-        return true;
-      };
-      for (int i = 0; ok && i < NBUF && i < n_q; ++i) ok = issue_s(i);
-      for (int i = 0; ok && i < n_q; ++i) {
-        ok = issue_g(i);
-        if (ok && i + NBUF < n_q) ok = issue_s(i + NBUF);
       }
-      if (ok) mma_commit(last_done);
       if (!ok) {
         raise_abort(abort_flag, p.status);
         mma_commit(drain);
         volatile int never = 0;
         mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp >= 2 + 4 * NWG) {
+    // ---------------------------------------------------------------- dV (first), dK (second) issuers
+    // dV, dK of tile i follow p_full(i): the gradient warps have read S^T(i), dP^T(i) and
+    // written P^T, dS^T over them.  Each thread's commit after its product is its share of
+    // the release of the Q/dO stage and of the buffer (q_empty, count 2).
+    if (lane == 0) {
+      const int w = warp - (2 + 4 * NWG);  // 0: dV += P^T dO, 1: dK += dS^T Q
+      constexpr uint32_t IDESC_G = idesc_bf16(KBM, D, true);
+      const uint64_t qt_desc_mn = sdesc_sw128(sbase + C::OFF_Q, KBN * 128, 1024);   // MN-major Q/dO tiles
+      const uint32_t d_tm = tmem + (w == 0 ? C::TM_DV : C::TM_DK);
+      const uint32_t a_tm = tmem + (w == 0 ? C::TM_S : C::TM_DP);
+      const uint32_t b_off = w == 0 ? C::QT_BYTES : 0;  // dO (for dV) or Q (for dK)
+      bool ok = true;
+      for (int i = 0; ok && i < n_q; ++i) {
+        const int st = i % C::NSTAGE, bf = i % NBUF;
+        ok = mbar_wait(&p_full[bf], (i / NBUF) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t b_desc = sdesc_add(qt_desc_mn, st * C::STAGE_BYTES + b_off);
+#pragma unroll
+        for (int kk = 0; kk < KBN / 16; ++kk)
+          mma_bf16_ts(d_tm, a_tm + bf * KBN + packed_col<NWG>(kk), sdesc_add(b_desc, kk * 16 * 128), IDESC_G,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&q_empty[st]);
+      }
+      if (ok) mma_commit(last_done);
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(&drain_g[w]);
+        volatile int never = 0;
+        mbar_wait(&drain_g[w], 0, &never);
       }
     }
   } else {
