@@ -362,11 +362,11 @@ __device__ __forceinline__ DqBlock dq_block_at(const BwdTcParams& p, int P, int 
 // Keys in tiles of 64.  Used at d = 128 (d = 64 has a kernel of its own below).  A block's
 // Q and dO are staged by TMA and copied into TMEM by warpgroup 0 right after the previous
 // block's last tile; the K/V ring runs on across blocks.
-// Warps: 0 TMA (K_j and V_j in one transaction), 1 MMA + TMEM, 2 .. 2+4*NWG-1 gradient
-// warps (warp w owns TMEM lanes 32*(w%4) ..; with two warpgroups WG k handles key
-// columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also writes the
-// CTA's Q and dO rows into TMEM).  NBUF S/dP buffers: with 2 the tensor cores compute
-// tile j+1 while tile j's dS is formed.
+// Warps: 0 TMA (K_j and V_j in one transaction), 1 TMEM and the S/dP products, 2 ..
+// 2+4*NWG-1 gradient warps (warp w owns TMEM lanes 32*(w%4) ..; with two warpgroups WG k
+// handles key columns [32k, 32k+32) of every tile, with one it handles all 64; WG 0 also
+// writes the CTA's Q and dO rows into TMEM), 2+4*NWG the dQ products.  NBUF S/dP buffers:
+// with 2 the tensor cores compute tile j+1 while tile j's dS is formed.
 // TMEM: S[b] cols [64b, 64b+64), dP[b] [64(NBUF+b), ...), dQ [128 NBUF, 128 NBUF + d),
 // then Q and dO (bf16 pairs, d/2 columns each: the A operands of S and dP).  dS (bf16)
 // is written over S[b]: warpgroup w packs its 32 keys into the first 16 columns of its own
@@ -385,7 +385,7 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
 
 template <int D, int NBUF, int NWG>
 struct DqCfg {
-  static constexpr int THREADS = 64 + 128 * NWG;
+  static constexpr int THREADS = 64 + 128 * NWG + 32;  // + the dQ-issuing warp
   static constexpr int KV_BYTES = QBN * D * 2;  // one K (or V) tile; a ring slot holds both
   static constexpr int NSLOT = 4;
   static constexpr int OFF_KV = 0;
@@ -394,8 +394,8 @@ struct DqCfg {
   static constexpr int OFF_QS = OFF_KV + NSLOT * 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_QS + 2 * (D / 64) * QS_HALF;
   // kv_full[NSLOT], kv_empty[NSLOT], q_full, s_full[NBUF], ds_full[NBUF], drain, last_done,
-  // qs_full, qs_empty
-  static constexpr int NBAR = 2 * NSLOT + 5 + 2 * NBUF;
+  // qs_full, qs_empty, drain_dq
+  static constexpr int NBAR = 2 * NSLOT + 6 + 2 * NBUF;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   // Q and dO of the CTA's rows (bf16 pairs, D/2 columns each) are the A operands of S, dP
@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
   uint64_t* last_done = drain + 1;
   uint64_t* qs_full = last_done + 1;   // a block's Q and dO staged in shared memory
   uint64_t* qs_empty = qs_full + 1;    // ... and copied from there into TMEM
+  uint64_t* drain_dq = qs_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
       mbar_init(&ds_full[i], 128 * NWG);
     }
     mbar_init(drain, 1);
+    mbar_init(drain_dq, 1);
     mbar_init(last_done, 1);
     mbar_init(qs_full, 1);
     mbar_init(qs_empty, 128);  // warpgroup 0 of the gradient warps
@@ -513,47 +515,59 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    // S/dP of tile t+NBUF follow dQ of tile t (S and dP of a buffer overwrite the dS that
-    // dQ reads); the S/dP lookahead runs into the next block once its Q and dO are in TMEM.
+    // ---------------------------------------------------------------- S, dP issuer
+    // S and dP of tile t go to buffer t % NBUF, over the dS of tile t - NBUF: issued once the
+    // dQ product of that tile has completed (its commit completes that tile's phase of
+    // kv_empty).  The first tile of a block waits for the block's Q and dO in TMEM.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(QBM, QBN, false);
-      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       // descriptors built once; each MMA only advances the start address
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);            // K-major
+      bool ok = true;
+      int t = 0;
+      for (int k = 0; ok && k < n_blk; ++k) {
+        const int n_kv = dq_block_at(p, P, cta, k, QBN).n_kv;
+        ok = mbar_wait(q_full, k & 1, abort_flag);
+        for (int j = 0; ok && j < n_kv; ++j, ++t) {
+          const int slot = t % C::NSLOT, bf = t % NBUF;
+          ok = mbar_wait(&kv_full[slot], (t / C::NSLOT) & 1, abort_flag) &&
+               (t < NBUF || mbar_wait(&kv_empty[(t - NBUF) % C::NSLOT], ((t - NBUF) / C::NSLOT) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
+          const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
+            mma_bf16_ts(tmem + C::TM_S + bf * QBN, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, boff), IDESC_S, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
+            mma_bf16_ts(tmem + C::TM_DP + bf * QBN, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, boff), IDESC_S,
+                        kk > 0);
+          }
+          mma_commit(&s_full[bf]);
+        }
+      }
+      if (!ok) {
+        raise_abort(abort_flag, p.status);
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, &never);
+      }
+    }
+  } else if (warp == 2 + 4 * NWG) {
+    // ---------------------------------------------------------------- dQ issuer
+    // dQ of tile t follows ds_full(t), which the gradient warps signal only after reading
+    // S(t), dP(t): those MMAs have completed, so this thread's commit after dQ(t) is the last
+    // use of K_t, V_t and of the buffer's dS, and frees both.  The first dQ of a block
+    // overwrites the accumulator: the gradient warps signal its ds_full only after their
+    // epilogue of the previous block has read it.
+    if (lane == 0) {
+      constexpr uint32_t IDESC_DQ = idesc_bf16(QBM, D, true);
       const uint64_t kv_desc_mn = sdesc_sw128(sbase + C::OFF_KV, QBN * 128, 1024);    // MN-major
       bool ok = true;
-      // S/dP cursor: block ks, tile js of it (n_ks tiles), global tile index ts
-      int ks = 0, js = 0, ts = 0;
-      int n_ks = n_blk > 0 ? dq_block_at(p, P, cta, 0, QBN).n_kv : 0;
-      auto issue_s = [&]() -> bool {
-        if (js == 0 && !mbar_wait(q_full, ks & 1, abort_flag)) return false;
-        const int slot = ts % C::NSLOT, bf = ts % NBUF;
-        if (!mbar_wait(&kv_full[slot], (ts / C::NSLOT) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t k_desc = sdesc_add(kv_desc_k, slot * 2 * C::KV_BYTES);
-        const uint64_t v_desc = sdesc_add(k_desc, C::KV_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
-          mma_bf16_ts(tmem + C::TM_S + bf * QBN, tmem + C::TM_Q + kk * 8, sdesc_add(k_desc, boff), IDESC_S, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t boff = (kk >> 2) * (QBN * 128) + (kk & 3) * 32;
-          mma_bf16_ts(tmem + C::TM_DP + bf * QBN, tmem + C::TM_DO + kk * 8, sdesc_add(v_desc, boff), IDESC_S, kk > 0);
-        }
-        mma_commit(&s_full[bf]);
-        ++ts;
-        if (++js == n_ks) {
-          js = 0;
-          ++ks;
-          n_ks = ks < n_blk ? dq_block_at(p, P, cta, ks, QBN).n_kv : 0;
-        }
-        return true;
-      };
-      auto s_left = [&]() { return ks < n_blk; };
-      for (int i = 0; ok && i < NBUF && s_left(); ++i) ok = issue_s();
       int t = 0;
       for (int k = 0; ok && k < n_blk; ++k) {
         const int n_kv = dq_block_at(p, P, cta, k, QBN).n_kv;
@@ -567,16 +581,15 @@ __global__ void __launch_bounds__(DqCfg<D, NBUF, NWG>::THREADS, NBUF == 1 ? 2 : 
           for (int kk = 0; kk < QBN / 16; ++kk)
             mma_bf16_ts(tmem + C::TM_DQ, tmem + C::TM_S + bf * QBN + packed_col<NWG>(kk),
                         sdesc_add(k_desc, kk * 16 * 128), IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&kv_empty[slot]);  // K_t, V_t no longer read
-          if (j + 1 == n_kv) mma_commit(last_done);  // this block's dQ is complete
-          if (s_left()) ok = issue_s();
+          mma_commit(&kv_empty[slot]);  // K_t, V_t and the buffer's dS no longer read
         }
+        if (ok) mma_commit(last_done);  // this block's dQ is complete
       }
       if (!ok) {
         raise_abort(abort_flag, p.status);
-        mma_commit(drain);
+        mma_commit(drain_dq);
         volatile int never = 0;
-        mbar_wait(drain, 0, &never);
+        mbar_wait(drain_dq, 0, &never);
       }
     }
   } else {
