@@ -81,47 +81,70 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeArgs a) {
   }
 }
 
+// Each thread converts kUnroll float4s per pass, all loads first.
+constexpr int kUnroll = 2;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) convert_kernel(int64_t n, const float* src, T* dst) {
   const int64_t n4 = n / 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n4; i += stride)
-    store4(dst + 4 * i, load4(src + 4 * i));
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i0 < n4; i0 += stride * kUnroll) {
+    float4 x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (i0 + u * stride < n4) x[u] = load4(src + 4 * (i0 + u * stride));
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (i0 + u * stride < n4) store4(dst + 4 * (i0 + u * stride), x[u]);
+  }
   if (blockIdx.x == 0 && threadIdx.x < n - 4 * n4) {
     const int64_t i = 4 * n4 + threadIdx.x;
     dst[i] = from_f32<T>(src[i]);
   }
 }
 
-unsigned grid_for(int64_t work_threads) {
-  int dev = 0, sms = 0;
+// One wave of resident CTAs (SM count x CTAs per SM at this kernel's register use), fewer
+// when the work is smaller; each thread then strides over the rest.
+template <typename K>
+unsigned grid_for(K kernel, int64_t work_threads) {
+  int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     sms = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm <= 0) per_sm = 1;
   const int64_t want = (work_threads + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+template <typename T, int D>
+void merge_launch(const MergeArgs& a, cudaStream_t s) {
+  const unsigned grid = grid_for(merge_kernel<T, D>, a.rows * (D / 4));
+  merge_kernel<T, D><<<grid, kThreads, 0, s>>>(a);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t s) {
-  const unsigned grid = grid_for(a.rows * (a.d / 4));
   if (dtype == 0) {
-    if (a.d == 64) merge_kernel<float, 64><<<grid, kThreads, 0, s>>>(a);
-    else merge_kernel<float, 128><<<grid, kThreads, 0, s>>>(a);
+    if (a.d == 64) merge_launch<float, 64>(a, s);
+    else merge_launch<float, 128>(a, s);
   } else {
-    if (a.d == 64) merge_kernel<__nv_bfloat16, 64><<<grid, kThreads, 0, s>>>(a);
-    else merge_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, s>>>(a);
+    if (a.d == 64) merge_launch<__nv_bfloat16, 64>(a, s);
+    else merge_launch<__nv_bfloat16, 128>(a, s);
   }
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_convert(int64_t n, const float* src, void* dst, int dtype, cudaStream_t s) {
-  const unsigned grid = grid_for(n / 4 > 0 ? n / 4 : 1);
-  if (dtype == 0) convert_kernel<float><<<grid, kThreads, 0, s>>>(n, src, static_cast<float*>(dst));
-  else convert_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(n, src, static_cast<__nv_bfloat16*>(dst));
+  const int64_t work = n / 4 > 0 ? (n / 4 + kUnroll - 1) / kUnroll : 1;
+  if (dtype == 0) {
+    convert_kernel<float><<<grid_for(convert_kernel<float>, work), kThreads, 0, s>>>(n, src, static_cast<float*>(dst));
+  } else {
+    convert_kernel<__nv_bfloat16><<<grid_for(convert_kernel<__nv_bfloat16>, work), kThreads, 0, s>>>(
+        n, src, static_cast<__nv_bfloat16*>(dst));
+  }
   count_launches(1);
   return cudaGetLastError();
 }
