@@ -89,9 +89,9 @@ typedef struct {
  * Out: o (device, desc->dtype), lse (device, float32, may be NULL to skip it).
  * bf16 with d in {64, 128} runs on the tensor cores: tcgen05 MMAs with float32
  * accumulation for both memories (the depth slots read by each query's position enter
- * as extra, block-masked key tiles of the same online softmax; slots not read are never
- * loaded), P rounded to bf16 for the PV products.  float32, and bf16 reading more than
- * 128 of a larger slot capacity, run on the CUDA cores in float32. */
+ * the same online softmax as one extra key step per 128 slots read, their products
+ * masked to the rows of each position's queries; slots not read are never loaded), P
+ * rounded to bf16 for the PV products.  float32 runs on the CUDA cores in float32. */
 moda_status moda_fwd(const moda_desc* desc, const void* q, const void* k, const void* v, const void* kd,
                      const void* vd, void* o, float* lse, void* stream);
 

@@ -1,6 +1,6 @@
 // MoDA forward on the sm_103a tensor cores: a persistent kernel with two ping-pong
 // query tiles per work unit and tcgen05 MMAs into TMEM fed by TMA, in which the
-// same-position depth slots enter as extra, block-masked key tiles.
+// same-position depth slots of all the tile's positions enter as one extra key step.
 //
 // Operation: "Mixture-of-Depths Attention", frame "One denominator allocates
 // probability across both memories" (Sec. 2.2, Algorithm 1): one softmax over the
@@ -14,17 +14,20 @@
 // loads a tile: Q [B][H][T][d] is described to the TMA unit as (d, H, T, B), so the
 // box walks the G heads fastest.
 //
-// Key tiles of a query tile t, in the order the online softmax takes them:
-//   depth tiles i = 0 .. n_d-1.  When every slot in memory is read (S_read = S), 128
-//     consecutive rows of the tile's positions' slabs (contiguous in memory):
-//     kd[b, g, p0 + t*P + kappa/S, kappa%S, :] for kappa = 128 i .. 128 i + 127, and row r
-//     sees kappa in [(r/G) S, (r/G) S + S).  Otherwise (a bounded slot buffer read in part)
-//     the S_read slots of the dpt = floor(128 / S_read) positions p0 + t*P + i*dpt .. + dpt
-//     - 1, one 3-D TMA box (channels, slots, positions), so key kappa is slot kappa %
-//     S_read of position i*dpt + kappa / S_read: slots not read are never loaded.  This is
-//     the same-position depth memory H_l of the slides' formulas, scored by the same MMA as
+// Key steps of a query tile t, in the order the online softmax takes them:
+//   depth steps i = 0 .. n_d-1 (n_d = ceil(S_read / 128), one unless more than 128 slots
+//     are read).  The read slots 128 i .. 128 i + w - 1 (w = min(S_read, 128)) of the
+//     tile's positions come in chunks of dpt = floor(128 / w) positions, one 3-D TMA box
+//     (channels, slots, positions) each: key kappa of chunk c is slot 128 i + kappa % w of
+//     local position c*dpt + kappa / w (slots past S_read read as zeros; slots never read
+//     are never loaded).  Chunk c's S = Q K_c^T and O += P V_c are tensor-core products
+//     over all 128 rows whose TMEM write-back is masked to the rows of the chunk's
+//     positions (the disable-output-lane operand), so every chunk writes the same S and
+//     reads the same P columns and the step's softmax covers all chunks at once: row r
+//     sees columns [(r/G - c*dpt) w, + w) of its own chunk's keys.  This is the
+//     same-position depth memory H_l of the slides' formulas, scored by the same MMAs as
 //     the sequence.
-//   sequence tiles j = 0 .. : keys 128 j .. 128 j + 127 of kv head g, causal mask: key
+//   sequence steps j = 0 .. : keys 128 j .. 128 j + 127 of kv head g, causal mask: key
 //               j is visible to position t when j <= t + delta and j < Tk.  A whole
 //               sequence has delta = 0 and Tk = T; a query chunk scored against the key
 //               chunk of an earlier range of positions (context parallelism) has the
@@ -57,8 +60,7 @@
 //               scale; P rounded to bf16 (d = 128: into the TMEM columns of S); O rescaled
 //               only when the running max of a row that already holds probability mass
 //               grows by more than 2^8 (exact: the final division uses the same stale
-//               max); a warp none of whose positions a depth tile covers writes P = 0
-//               without reading S.  Then the epilogue o = O / l.
+//               max).  Then the epilogue o = O / l.
 //
 // TMEM columns, d = 128: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512); P is
 // packed bf16 in the first 64 columns of S_t.  d = 64: per tile t, S_t [256t, 256t+128),
@@ -121,9 +123,11 @@ struct FwdTcParams {
   int n_pb;     // position blocks (of 2P positions) per (b, kv head)
   int n_units;  // B * Hkv * n_pb
   int n_cta;    // persistent CTAs
-  int packed;   // 1: every slot is read, depth keys packed over positions (2-D rows)
-  int dpt;      // positions per depth key tile when not packed: floor(128 / S_read)
-  int n_d;      // depth key tiles per query tile: ceil(P*S / 128) packed, else ceil(P / dpt)
+  int n_d;      // depth steps per query tile: ceil(S_read / 128) (0 without depth slots)
+  int w;        // slots of a position per depth step: min(S_read, 128)
+  int dpt;      // positions per depth chunk: floor(128 / w)
+  int n_ch;     // depth chunks per depth step: ceil(P / dpt)
+  int nd_keys;  // keys of a depth chunk's products: dpt * w rounded up to 16
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -134,8 +138,19 @@ struct Unit {
   int b, g, bg, p0;
   int nt[2];     // sequence key tiles each query tile needs (0: tile beyond T)
   int ns[2];     // steps (depth + sequence key tiles) of each query tile (0: tile beyond T)
-  int nd_items;  // K/V items of the depth steps
 };
+
+// Output-lane mask of TMEM rows [lo, hi) for a masked MMA: bit i of m[q] set leaves lane
+// 32 q + i unwritten.
+__device__ __forceinline__ void rows_mask(int lo, int hi, uint32_t (&m)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int a = min(max(lo - 32 * q, 0), 32), b = min(max(hi - 32 * q, 0), 32);
+    const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+    const uint32_t below_a = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+    m[q] = ~(below_b & ~below_a);
+  }
+}
 
 // Units a CTA processes: the unit list in heaviest-first order, dealt round-robin with the
 // direction reversed every round (snake), so every CTA gets a similar amount of work.
@@ -160,13 +175,61 @@ __device__ __forceinline__ Unit unit_at(const FwdTcParams& p, int c, int k) {
   u.nt[1] = (u.p0 + p.P < p.T) ? min((end - 1 + p.delta) / BN + 1, nk) : 0;
   u.ns[0] = p.n_d + u.nt[0];
   u.ns[1] = u.nt[1] > 0 ? p.n_d + u.nt[1] : 0;
-  u.nd_items = p.n_d * (u.nt[1] > 0 ? 4 : 2);
   return u;
 }
 
-// K/V items of a unit, in the order the loader issues them: per depth step i, K_0, K_1,
-// V_0, V_1 (K_0, V_0 when tile 1 is empty); then per sequence step j, K_j, V_j shared
-// by both query tiles.
+// K/V items of a unit, in the order the loader issues them (with per = n_ch * tw items of
+// one kind per depth step, tw = 2 query tiles or 1 when tile 1 is empty):
+//   depth step i:   K of chunk c of tile t at 2 i per + c tw + t (the two tiles' chunks
+//                   alternate), then V likewise at + per;
+//   sequence steps: K_j, V_j, each shared by both query tiles.
+// With one MMA issuer per query tile (d = 64: S of the next step issued before the P V of
+// this one) the sequence's K_0 is hoisted between the K and the V items of the last depth
+// step ("hoist"); the single issuer (d = 128) takes both tiles' depth P V before S of the
+// next step, and K_0 stays in its place.
+// Every consumer takes its items in load order, and an issuer's consecutive items are at
+// most two apart within a unit (a unit's first item is waited for after its Q tile, which
+// the loader issues after every item of the previous unit).  So when an issuer waits for
+// item x, the loader has issued item x - NSLOT, which it does only after item x - 2 NSLOT
+// was released: the earlier use of x's full barrier (even and odd loads of a slot have a
+// barrier each) has completed, and the parity wait cannot pass on it.
+struct Items {
+  int base, tw, per, n_d, hoist, nd;  // nd: items of the depth steps (with a hoisted K_0)
+  __device__ __forceinline__ Items(const FwdTcParams& p, const Unit& u, int b, bool split)
+      : base(b), tw(u.nt[1] > 0 ? 2 : 1), per(p.n_ch * tw), n_d(p.n_d), hoist(split && p.n_d > 0 ? 1 : 0),
+        nd(p.n_d > 0 ? 2 * p.n_d * per + hoist : 0) {}
+  __device__ __forceinline__ int dk(int i, int c, int t) const { return base + 2 * i * per + c * tw + t; }
+  __device__ __forceinline__ int dv(int i, int c, int t) const {
+    return base + 2 * i * per + per + (i == n_d - 1 ? hoist : 0) + c * tw + t;
+  }
+  __device__ __forceinline__ int sk(int j) const {
+    return hoist ? (j == 0 ? base + 2 * (n_d - 1) * per + per : base + nd + 2 * j - 1) : base + nd + 2 * j;
+  }
+  __device__ __forceinline__ int sv(int j) const { return base + nd + 2 * j + 1 - hoist; }
+  // first item of the next unit, after m sequence steps
+  __device__ __forceinline__ int end(int m) const { return base + nd + 2 * m - hoist; }
+  // what item r (from base) is: kind 0/1 depth K/V of step i, chunk c, tile t; 2/3
+  // sequence K/V of step j
+  __device__ __forceinline__ void decode(int r, int& kind, int& i, int& c, int& t, int& j) const {
+    i = c = t = j = 0;
+    if (r < nd) {
+      i = min(r / (2 * per), n_d - 1);
+      const int rem = r - 2 * i * per, lastd = i == n_d - 1 ? hoist : 0;
+      if (lastd && rem == per) {
+        kind = 2;  // the hoisted K_0
+        return;
+      }
+      kind = rem < per ? 0 : 1;
+      const int e = rem < per ? rem : rem - per - lastd;
+      c = e / tw;
+      t = e % tw;
+    } else {
+      const int q = r - nd + hoist;  // index in K_0 V_0 K_1 V_1 ...
+      j = q >> 1;
+      kind = 2 + (q & 1);
+    }
+  }
+};
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
   *abort_flag = 1;
@@ -245,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (p.n_d > 0 && !p.packed && p.dpt * p.S_read < BN) {
-    // rows of a depth key tile past its dpt * S_read keys are seen by no row, but enter
-    // the P V product with P = 0: they must hold finite numbers, so the ring starts zeroed
+  if (p.n_d > 0 && p.dpt * p.w < p.nd_keys) {
+    // rows of a depth chunk past its dpt * w keys are seen by no row, but enter the P V
+    // product with P = 0: they must hold finite numbers, so the ring starts zeroed
     // (afterwards they hold loaded keys and values)
     for (int i = threadIdx.x; i < C::NSLOT * C::TILE_BYTES / 16; i += kThreads)
       st_shared_v4(sbase + C::OFF_KV + i * 16, make_uint4(0, 0, 0, 0));
@@ -284,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             q_issued1 = k + 1;
         }
-        const int two = u.nt[1] > 0 ? 2 : 1;
-        const int n_items = u.nd_items + 2 * max(u.nt[0], u.nt[1]);
+        const Items itl(p, u, 0, C::SPLIT);
+        const int n_items = itl.end(max(u.nt[0], u.nt[1]));
         for (int r = 0; ok && r < n_items; ++r, ++it) {
           const int slot = it % C::NSLOT, use = it / C::NSLOT;
           if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
@@ -294,30 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* dst = smem + C::OFF_KV + slot * C::TILE_BYTES;
           uint64_t* full = &kv_full[2 * slot + (use & 1)];
-          if (r < u.nd_items) {
-            // depth step i: K of each query tile, then V of each; rows past dpt*S_read keep
-            // what the slot held (finite: zeroed at start, then loaded keys and values) and
-            // are seen by no row
-            const int i = r / (2 * two), w = r % (2 * two);
-            const int kind = w / two, t = w % two;
+          int kind, i, c, t, j;
+          itl.decode(r, kind, i, c, t, j);
+          if (kind < 2) {
+            // depth chunk c of step i of tile t: dpt positions x w slots; rows past dpt * w
+            // keep what the slot held (finite: zeroed at start, then loaded keys and values)
+            // and are seen by no row
             const CUtensorMap* map = kind ? &tmVd : &tmKd;
-            if (p.packed) {
-              const int row = (u.bg * p.T + u.p0 + t * p.P) * p.S + i * BN;
-              mbar_arrive_expect_tx(full, C::TILE_BYTES);
+            const int pos0 = u.bg * p.T + u.p0 + t * p.P + c * p.dpt;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(D) * p.w * p.dpt * 2);
 #pragma unroll
-              for (int h = 0; h < D / 64; ++h)
-                tma_load_2d_hint(dst + h * (BN * 128), map, full, h * 64, row, pol_once);
-            } else {
-              const int pos0 = u.bg * p.T + u.p0 + t * p.P + i * p.dpt;
-              mbar_arrive_expect_tx(full, static_cast<uint32_t>(D) * p.S_read * p.dpt * 2);
-#pragma unroll
-              for (int h = 0; h < D / 64; ++h)
-                tma_load_3d_hint(dst + h * (BN * 128), map, full, h * 64, 0, pos0, pol_once);
-            }
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d_hint(dst + h * (BN * 128), map, full, h * 64, i * BN, pos0, pol_once);
           } else {
             mbar_arrive_expect_tx(full, C::TILE_BYTES);
-            const int j = (r - u.nd_items) >> 1, kind = (r - u.nd_items) & 1;
-            const CUtensorMap* map = kind ? &tmV : &tmK;
+            const CUtensorMap* map = kind == 3 ? &tmV : &tmK;
 #pragma unroll
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(dst + h * (BN * 128), map, full, h * 64, j * BN, u.bg);
@@ -342,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
+      const uint32_t idesc_d = idesc_bf16(BM, p.nd_keys, false);  // a depth chunk's S
       const uint64_t q_desc0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);        // K-major (K tiles)
       const uint64_t kv_desc_v = sdesc_sw128(sbase + C::OFF_KV, BN * 128, 1024);  // MN-major (V tiles)
@@ -382,89 +437,122 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      // The issuing warp is on the critical path between MMA groups: item indices are kept
-      // incremental, and the depth and sequence steps have a loop each.
+      // The issuing warp is on the critical path between MMA groups: the depth and sequence
+      // steps have a loop each.
       for (int k = 0; ok && k < n_c; ++k) {
         const Unit u = unit_at(p, cta, k);
         const int nA = u.ns[0], nB = u.ns[1];
         const bool two = nB > 0;
-        const int sbase = base + u.nd_items;  // first sequence item
         ok = warp_wait(&q_full[0], k & 1, abort_flag) && warp_wait(&q_full[1], k & 1, abort_flag);
         if (!ok) break;
         if (!two) mma_commit_warp(&q_empty[1]);  // tile 1 unused in this unit
+        const Items it(p, u, base, false);
+        const int tw = two ? 2 : 1;
+        // S of depth step i: chunk by chunk, each tile's product into its S, masked to the
+        // chunk's rows, then a commit per tile
+        auto depth_s = [&](int i) -> bool {
+          for (int c = 0; c < p.n_ch; ++c) {
+            uint32_t mask[4];
+            rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
+            for (int t = 0; t < tw; ++t) {
+              const int item = it.dk(i, c, t);
+              if (!wait_item(item)) return false;
+              tc_fence_after();
+              const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
+              const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
+              if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_bf16_ss_mask(tmem + C::tm_s(t), sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                                   sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), idesc_d, kk > 0, mask);
+              }
+              __syncwarp();
+              release(item);
+            }
+          }
+          for (int t = 0; t < tw; ++t) mma_commit_warp(&s_full[t]);
+          return true;
+        };
+        // O_t += P_t V of depth step i once both tiles' P are written: chunk by chunk, each
+        // product masked to the chunk's rows (step 0 starts each row's O)
+        auto depth_pv = [&](int i) -> bool {
+          for (int t = 0; t < tw; ++t) {
+            uint32_t& pc = t ? pcnt1 : pcnt0;
+            if (!warp_wait(&p_full[t], pc & 1, abort_flag) ||
+                (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag)))
+              return false;
+            ++pc;
+          }
+          tc_fence_after();
+          for (int c = 0; c < p.n_ch; ++c) {
+            uint32_t mask[4];
+            rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
+            for (int t = 0; t < tw; ++t) {
+              const int item = it.dv(i, c, t);
+              if (!wait_item(item)) return false;
+              tc_fence_after();
+              const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
+              if (elect_one()) {
+                for (int kk = 0; kk < p.nd_keys / 16; ++kk)
+                  mma_bf16_ts_mask(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, sdesc_add(v_desc, kk * 16 * 128),
+                                   IDESC_O, (i > 0 || kk > 0) ? 1u : 0u, mask);
+              }
+              __syncwarp();
+              release(item);
+            }
+          }
+          return true;
+        };
         // S of step 0
-        {
-          const int ka = p.n_d > 0 ? base : sbase;
-          const int kb = p.n_d > 0 ? base + 1 : sbase;
-          if (!wait_item(ka)) {
+        if (p.n_d > 0) {
+          if (!depth_s(0)) {
+            ok = false;
+            break;
+          }
+        } else {
+          if (!wait_item(it.sk(0))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(0, ka);
+          issue_s(0, it.sk(0));
           if (nA == 1) mma_commit_warp(&q_empty[0]);
           if (two) {
-            if (kb != ka && !wait_item(kb)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(1, kb);
+            issue_s(1, it.sk(0));
             if (nB == 1) mma_commit_warp(&q_empty[1]);
-            if (kb != ka) release(kb);
           }
-          release(ka);
+          release(it.sk(0));
         }
-        // ---- depth steps: each query tile has K and V items of its own
+        // ---- depth steps: each query tile has K and V items of its own.  Both tiles' P V
+        // first, then S of step i+1 (the next depth step, or the first sequence step,
+        // whose K both tiles read): the items are consumed in the order they are loaded.
         for (int i = 0; ok && i < p.n_d; ++i) {
-          const int stride = two ? 4 : 2;
-          const int va = base + stride * i + (two ? 2 : 1), vb = va + 1;
-          const bool last = i + 1 == p.n_d;
-          const int ka = last ? sbase : base + stride * (i + 1);
-          const int kb = last ? sbase : ka + 1;
-          if (!wait_item(va) || !warp_wait(&p_full[0], pcnt0 & 1, abort_flag) ||
-              (i == 0 && k > 0 && !warp_wait(&o_free[0], (k - 1) & 1, abort_flag))) {
+          if (!depth_pv(i)) {
             ok = false;
             break;
           }
-          ++pcnt0;
-          tc_fence_after();
-          issue_pv(0, va, i > 0, i + 1 == nA);
-          if (!wait_item(ka)) {
-            ok = false;
-            break;
+          if (i + 1 < p.n_d) {
+            if (!depth_s(i + 1)) {
+              ok = false;
+              break;
+            }
+          } else {
+            if (!wait_item(it.sk(0))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, it.sk(0));
+            if (two) issue_s(1, it.sk(0));
+            release(it.sk(0));
           }
-          tc_fence_after();
-          issue_s(0, ka);
           if (i + 2 == nA) mma_commit_warp(&q_empty[0]);
-          if (two) {
-            if (!wait_item(vb) || !warp_wait(&p_full[1], pcnt1 & 1, abort_flag) ||
-                (i == 0 && k > 0 && !warp_wait(&o_free[1], (k - 1) & 1, abort_flag))) {
-              ok = false;
-              break;
-            }
-            ++pcnt1;
-            tc_fence_after();
-            issue_pv(1, vb, i > 0, i + 1 == nB);
-            release(vb);
-          }
-          release(va);
-          if (two) {
-            if (kb != ka && !wait_item(kb)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(1, kb);
-            if (i + 2 == nB) mma_commit_warp(&q_empty[1]);
-            if (kb != ka) release(kb);
-          }
-          release(ka);
+          if (two && i + 2 == nB) mma_commit_warp(&q_empty[1]);
         }
         // ---- sequence steps: K and V shared by both tiles; S of the first was issued above
         const int mA = nA - p.n_d, mB = two ? nB - p.n_d : 0, m = max(mA, mB);
         for (int j = 0; ok && j < m; ++j) {
-          const int iv = sbase + 2 * j + 1, ik = iv + 1;
+          const int iv = it.sv(j), ik = it.sk(j + 1);
           const bool first = p.n_d == 0 && j == 0;  // first PV of the unit
           if (!wait_item(iv)) {
             ok = false;
@@ -507,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (next) release(ik);  // K_{j+1}: every S reading it is issued
         }
-        base = sbase + 2 * m;
+        base = it.end(m);
       }
       if (!ok) {
         raise_abort(abort_flag, p.status);
@@ -526,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = warp - 1;
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false);
       constexpr uint32_t IDESC_O = idesc_bf16(BM, D, true);
-      
+      const uint32_t idesc_d = idesc_bf16(BM, p.nd_keys, false);  // a depth chunk's S
       const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + t * C::TILE_BYTES, 16, 1024);
       const uint64_t kv_desc_k = sdesc_sw128(sbase + C::OFF_KV, 16, 1024);        // K-major (K tiles)
       const uint64_t kv_desc_v = sdesc_sw128(sbase + C::OFF_KV, BN * 128, 1024);  // MN-major (V tiles)
@@ -569,20 +657,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int k = 0; ok && k < n_c; ++k) {
         const Unit u = unit_at(p, cta, k);
-        const bool two = u.ns[1] > 0;
         const int n_t = t ? u.ns[1] : u.ns[0];
         const int nt_other = t ? u.nt[0] : u.nt[1];  // sequence tiles of the other query tile
-        const int sbase = base + u.nd_items, st = two ? 4 : 2;
-        // K and V items of step i of this tile, and whether the other tile reads them too
-        auto kv = [&](int i, int& ki, int& vi) -> bool {
+        const Items it(p, u, base, true);
+        // S of step i: a depth step's chunks (each masked to its rows, one commit), or the
+        // sequence tile's K, read by the other tile too while it has that tile
+        auto step_s = [&](int i) -> bool {
           if (i < p.n_d) {
-            ki = base + st * i + t;
-            vi = base + st * i + (two ? 2 : 1) + t;
-            return false;
+            for (int c = 0; c < p.n_ch; ++c) {
+              const int item = it.dk(i, c, t);
+              if (!wait_item(item)) return false;
+              tc_fence_after();
+              uint32_t mask[4];
+              rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
+              const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
+              if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_bf16_ss_mask(s_tm, sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                                   sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), idesc_d, kk > 0, mask);
+              }
+              __syncwarp();
+              release(item, false);
+            }
+            mma_commit_warp(&s_full[t]);
+            ++scnt;
+            return true;
           }
-          ki = sbase + 2 * (i - p.n_d);
-          vi = ki + 1;
-          return i - p.n_d < nt_other;
+          const int ki = it.sk(i - p.n_d);
+          if (!wait_item(ki)) return false;
+          tc_fence_after();
+          issue_s(ki);
+          release(ki, i - p.n_d < nt_other);
+          return true;
+        };
+        // PV of step i once P is written: per depth chunk, masked to its rows (step 0 starts
+        // each row's O); then pv_done
+        auto step_pv = [&](int i) -> bool {
+          if (!warp_wait(&p_full[t], pcnt & 1, abort_flag) ||
+              (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag)))
+            return false;
+          ++pcnt;
+          tc_fence_after();
+          if (i < p.n_d) {
+            for (int c = 0; c < p.n_ch; ++c) {
+              const int item = it.dv(i, c, t);
+              if (!wait_item(item)) return false;
+              tc_fence_after();
+              uint32_t mask[4];
+              rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
+              const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
+              if (elect_one()) {
+                for (int kk = 0; kk < p.nd_keys / 16; ++kk)
+                  mma_bf16_ts_mask(o_tm, p_tm + kk * 8, sdesc_add(v_desc, kk * 16 * 128), IDESC_O,
+                                   (i > 0 || kk > 0) ? 1u : 0u, mask);
+              }
+              __syncwarp();
+              release(item, false);
+            }
+            mma_commit_warp(&pv_done[t]);
+            return true;
+          }
+          const int vi = it.sv(i - p.n_d);
+          if (!wait_item(vi)) return false;
+          tc_fence_after();
+          issue_pv(vi, i > 0);
+          release(vi, i - p.n_d < nt_other);
+          return true;
         };
         ok = warp_wait(&q_full[t], k & 1, abort_flag);
         if (!ok) break;
@@ -590,63 +731,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_warp(&q_empty[t]);  // tile unused in this unit
         } else {
           // S of step 0
-          int ki, vi;
-          bool sh = kv(0, ki, vi);
-          if constexpr (C::SPLIT) {
-            if (scnt > 0 && !warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag)) ok = false;
-          }
-          if (ok && !wait_item(ki)) ok = false;
-          if (ok) {
-            tc_fence_after();
-            issue_s(ki);
-            if (n_t == 1) mma_commit_warp(&q_empty[t]);
-            release(ki, sh);
-          }
+          if (scnt > 0 && !warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag)) ok = false;
+          if (ok) ok = step_s(0);
+          if (ok && n_t == 1) mma_commit_warp(&q_empty[t]);
           for (int i = 0; ok && i < n_t; ++i) {
-            const bool more = i + 1 < n_t;
-            int kn = 0, vn = 0;
-            const bool sh_n = more ? kv(i + 1, kn, vn) : false;
-            sh = kv(i, ki, vi);
-            if constexpr (C::SPLIT) {
-              // S of step i+1 as soon as the softmax has read S of step i
-              if (more) {
-                if (!warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag) || !wait_item(kn)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                issue_s(kn);
-                if (i + 2 == n_t) mma_commit_warp(&q_empty[t]);
-                release(kn, sh_n);
-              }
-            }
-            // PV of step i once P is written
-            if (!wait_item(vi) || !warp_wait(&p_full[t], pcnt & 1, abort_flag) ||
-                (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag))) {
+            // S of step i+1 as soon as the softmax has read S of step i (PV of step i goes
+            // first when both are depth steps: step i+1's K items are loaded after step i's
+            // V items)
+            const bool pv_first = i + 1 < p.n_d;
+            if (pv_first && !step_pv(i)) {
               ok = false;
               break;
             }
-            ++pcnt;
-            tc_fence_after();
-            issue_pv(vi, i > 0);
-            release(vi, sh);
-            if constexpr (!C::SPLIT) {
-              // S of step i+1 overwrites P of step i: in-order execution of this thread's
-              // MMAs makes that safe once the PV reading it is issued
-              if (more) {
-                if (!wait_item(kn)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                issue_s(kn);
-                if (i + 2 == n_t) mma_commit_warp(&q_empty[t]);
-                release(kn, sh_n);
+            if (i + 1 < n_t) {
+              if (!warp_wait(&s_free[t], (scnt - 1) & 1, abort_flag) || !step_s(i + 1)) {
+                ok = false;
+                break;
               }
+              if (i + 2 == n_t) mma_commit_warp(&q_empty[t]);
+            }
+            if (!pv_first && !step_pv(i)) {
+              ok = false;
+              break;
             }
           }
         }
-        base = sbase + 2 * max(u.nt[0], u.nt[1]);
+        base = it.end(max(u.nt[0], u.nt[1]));
       }
       if (!ok) {
         raise_abort(abort_flag, p.status);
@@ -666,8 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_tmem = tmem + lane_base + C::tm_p(t);
     const uint32_t o_tmem = tmem + lane_base + C::tm_o(t);
     const int pl = r / p.G, hl = r - pl * p.G;  // local position and head of row r
-    // positions this warp's rows cover (for skipping depth tiles that miss them all)
-    const int wp_lo = (wq * 32) / p.G, wp_hi = min(wq * 32 + 31, p.P * p.G - 1) / p.G;
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, jcnt = 0;  // s_full phases consumed, PVs of this tile so far
     uint32_t ucnt = 0;            // units with keys for this tile so far (pv_done phases, d = 128)
@@ -691,41 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool depth = j < p.n_d;
         int lo, hi;  // visible columns [lo, hi) of this row in this key tile
         if (depth) {
-          // key offset of local position x in this depth tile: x * S - 128 j (packed) or
-          // (x - j dpt) S_read; visible when inside [0, 128) (packed) or x in the tile's dpt
-          const int d0 = j * p.dpt;  // first position of this depth tile (not packed)
-          const bool skip = p.packed ? (wp_hi * p.S + p.S <= j * BN || wp_lo * p.S >= j * BN + BN)
-                                     : (wp_hi < d0 || wp_lo >= d0 + p.dpt);
-          if (skip) {
-            // no position of this warp has keys in this depth tile: P = 0
-            if constexpr (C::SPLIT) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&s_free[t]);
-              if (j > 0) {  // P_t is still read by the previous PV until it completes
-                ok = warp_wait(&pv_done[t], (jcnt - 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-              }
-            }
-            uint32_t z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0u;
-            tmem_st32(p_tmem, z);
-            tmem_st32(p_tmem + 32, z);
-            tc_fence_before();
-            mbar_arrive(&p_full[t]);
-            ++jcnt;
-            continue;
-          }
-          if (p.packed) {
-            lo = valid ? pl * p.S - j * BN : BN;
-            hi = valid ? lo + p.S : BN;
-          } else {
-            const bool in = valid && pl >= d0 && pl < d0 + p.dpt;
-            lo = in ? (pl - d0) * p.S_read : BN;
-            hi = in ? lo + p.S_read : BN;
-          }
+          // the row's own position's slots 128 j .. 128 j + w - 1 (those below S_read) in
+          // its chunk: local position x of chunk x / dpt has keys [(x % dpt) w, + w)
+          lo = valid ? (pl % p.dpt) * p.w : BN;
+          hi = valid ? lo + min(p.w, p.S_read - j * BN) : BN;
         } else {
           // keys kb + c with c < hi are visible: c <= pos + delta - kb and kb + c < Tk
           const int kb = (j - p.n_d) * BN;
@@ -906,23 +983,15 @@ bool make_kv_map(CUtensorMap* map, const void* base, int D, int T, int groups) {
   return encode(map, base, 3, dims, strides, box);
 }
 
-// Depth slabs [B*Hkv*T*S rows][D] bf16 as a 2-D tensor (every slot read); box 64 x 128
-// (128 consecutive (position, slot) rows); rows past the end read as zeros.
-bool make_depth_rows_map(CUtensorMap* map, const void* base, int D, int64_t rows) {
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
-  return encode(map, base, 2, dims, strides, box);
-}
-
 // Depth slabs [B*Hkv*T positions][C slots][D] bf16 as a 3-D tensor (D, S_read, positions):
-// slots from S_read on lie outside it and are never read; box 64 x S_read x dpt (the dpt
-// positions of a depth key tile); positions past the end read as zeros.
-bool make_depth_map(CUtensorMap* map, const void* base, int D, int S_read, int C, int64_t npos, int dpt) {
+// slots from S_read on lie outside it and are never loaded (a box reaching past S_read, or
+// past the last position, reads zeros there); box 64 x w x dpt (the w slots of the dpt
+// positions of a depth chunk).
+bool make_depth_map(CUtensorMap* map, const void* base, int D, int S_read, int C, int64_t npos, int w, int dpt) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S_read),
                               static_cast<cuuint64_t>(npos)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(C) * D * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(S_read), static_cast<cuuint32_t>(dpt)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(w), static_cast<cuuint32_t>(dpt)};
   return encode(map, base, 3, dims, strides, box);
 }
 
@@ -965,9 +1034,12 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   p.n_cta = std::min(p.n_units, sms);
-  p.packed = pr.S > 0 && pr.S_read == pr.S;
-  p.dpt = pr.S > 0 ? BN / pr.S_read : 1;
-  p.n_d = pr.S == 0 ? 0 : p.packed ? (p.P * pr.S + BN - 1) / BN : (p.P + p.dpt - 1) / p.dpt;
+  const bool depth = pr.S > 0 && pr.S_read > 0;
+  p.w = depth ? std::min(pr.S_read, BN) : 1;
+  p.dpt = BN / p.w;
+  p.n_d = depth ? (pr.S_read + BN - 1) / BN : 0;
+  p.n_ch = depth ? (p.P + p.dpt - 1) / p.dpt : 0;
+  p.nd_keys = std::min(BN, (p.dpt * p.w + 15) / 16 * 16);
   p.scale_log2 = pr.scale_log2;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
@@ -976,13 +1048,11 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
   if (!make_q_map(&tq, a.q, D, pr.T, pr.H, pr.B, p.P, pr.G) || !make_kv_map(&tk, a.k, D, pr.Tk, pr.B * pr.Hkv) ||
       !make_kv_map(&tv, a.v, D, pr.Tk, pr.B * pr.Hkv))
     return cudaErrorInvalidValue;
-  if (pr.S > 0) {
+  if (depth) {
     const int64_t npos = static_cast<int64_t>(pr.B) * pr.Hkv * pr.T;
-    const bool okd = p.packed ? make_depth_rows_map(&tkd, a.kd, D, npos * pr.S) &&
-                                    make_depth_rows_map(&tvd, a.vd, D, npos * pr.S)
-                              : make_depth_map(&tkd, a.kd, D, pr.S_read, pr.S, npos, p.dpt) &&
-                                    make_depth_map(&tvd, a.vd, D, pr.S_read, pr.S, npos, p.dpt);
-    if (!okd) return cudaErrorInvalidValue;
+    if (!make_depth_map(&tkd, a.kd, D, pr.S_read, pr.S, npos, p.w, p.dpt) ||
+        !make_depth_map(&tvd, a.vd, D, pr.S_read, pr.S, npos, p.w, p.dpt))
+      return cudaErrorInvalidValue;
   } else {
     tkd = tk;  // never read
     tvd = tv;
@@ -998,12 +1068,9 @@ cudaError_t launch(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool fwd_sm103_supported(const Problem& p) {
-  // depth rows (all slots read) or positions (a part read) are addressed with 32-bit TMA
-  // coordinates; a position's read slots fit one depth key tile when only a part is read
+  // depth positions are addressed with 32-bit TMA coordinates
   const int64_t npos = static_cast<int64_t>(p.B) * p.Hkv * p.T;
-  const bool packed = p.S_read == p.S;
-  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && npos * (packed ? p.S : 1) < (int64_t(1) << 31) &&
-         (p.S == 0 || packed || p.S_read <= BN);
+  return (p.d == 64 || p.d == 128) && p.G >= 1 && p.G <= kMaxG && npos < (int64_t(1) << 31);
 }
 
 cudaError_t launch_fwd_sm103(const FwdArgs& a, cudaStream_t s) {

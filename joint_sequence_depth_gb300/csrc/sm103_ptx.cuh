@@ -190,6 +190,29 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same two products with some lanes of D left as they are: bit i of mask[w] set keeps
+// TMEM lane 32 w + i of D unwritten (the disable-output-lane operand of tcgen05.mma).  The
+// tensor core still forms every row; only the write-back is masked.
+__device__ __forceinline__ void mma_bf16_ss_mask(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate, const uint32_t (&mask)[4]) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, {%5, %6, %7, %8}, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(mask[0]), "r"(mask[1]), "r"(mask[2]), "r"(mask[3])
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ts_mask(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate, const uint32_t (&mask)[4]) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, {%5, %6, %7, %8}, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(mask[0]), "r"(mask[1]), "r"(mask[2]), "r"(mask[3])
+      : "memory");
+}
+
 // One lane of a converged warp (the lowest active lane, the same one at every call when the
 // whole warp is active).  MMA-issuing roles run their loops warp-wide and issue each group
 // of tcgen05 instructions from the elected lane: a loop that runs in one lane alone issues
