@@ -349,6 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const Items itl(p, u, 0, C::SPLIT);
         const int n_items = itl.end(max(u.nt[0], u.nt[1]));
+        // d = 128: while this unit's sequence tiles load, one depth chunk of the next unit
+        // per item is prefetched into L2 (the 5-slot ring holds few bytes in flight during
+        // a depth step; at d = 64 the 12-slot ring does, and the prefetch only displaced
+        // sequence K/V from L2)
+        const bool pf_next = D == 128 && p.n_d > 0 && k + 1 < n_c;
+        const Unit un = pf_next ? unit_at(p, cta, k + 1) : u;
+        const Items itn(p, un, 0, C::SPLIT);
+        int pf = 0;
         for (int r = 0; ok && r < n_items; ++r, ++it) {
           const int slot = it % C::NSLOT, use = it / C::NSLOT;
           if (use > 0 && !mbar_wait(&kv_empty[slot], (use - 1) & 1, abort_flag)) {
@@ -375,6 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(dst + h * (BN * 128), map, full, h * 64, j * BN, u.bg);
+          }
+          if (pf_next && r >= itl.nd && pf < itn.nd) {
+            // (at d = 128 the depth items are all of the next unit's first itn.nd items)
+            int kn, in_, cn, tn, jn;
+            itn.decode(pf++, kn, in_, cn, tn, jn);
+            const CUtensorMap* mp = kn ? &tmVd : &tmKd;
+            const int ps = un.bg * p.T + un.p0 + tn * p.P + cn * p.dpt;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) tma_prefetch_3d(mp, h * 64, in_ * BN, ps);
           }
           issued = it + 1;
         }
