@@ -40,6 +40,8 @@ SMALL = [
     ("bf16_d128_g1_blocks_gt_sms", 2, 16, 16, 700, 128, 4, bf16),
     ("bf16_d128_g4_blocks_gt_sms", 2, 16, 4, 1100, 128, 3, bf16),
     ("bf16_d64_g4_blocks_gt_sms", 2, 16, 4, 1100, 64, 3, bf16),
+    # more than 128 slots read (the forward takes two depth key steps)
+    ("bf16_d64_g4_slots_gt_tile", 1, 4, 1, 150, 64, 160, bf16),
 ]
 
 
