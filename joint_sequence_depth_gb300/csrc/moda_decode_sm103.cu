@@ -9,9 +9,10 @@
 // its kv head.  The keys are split (flash-decoding): CTA (split, b*Hkv + g) streams its
 // key range in sub-tiles of 128 keys through one K and one V slot (TMA, 128-byte swizzle,
 // K of the next sub-tile loading while P V of this one runs); the extra
-// last split of each (b, g) takes the S depth slots.  Per sub-tile, lane = key for the
-// scores (q in shared memory, read as broadcasts), then lane = d/32 output columns for
-// P V (P broadcast by shuffles).  Each warp keeps, per head, a running max,
+// last split of each (b, g) takes the S depth slots.  Per sub-tile, the scores of the G
+// heads are one tensor-core product S^T = K q^T (M = 128 keys, N = 16 with the heads past
+// G zero, into 16 TMEM columns), read back with lane = key; then lane = d/32 output
+// columns for P V on the CUDA cores (P read back from shared memory as broadcasts).  Each warp keeps, per head, a running max,
 // per-lane denominators and its output numerator; the CTA merges its warps and writes one
 // partial state {max, sum, numerator} per head to a float32 workspace.  A second kernel
 // merges the splits of each (b, h) by the same online rule and divides once.
@@ -49,16 +50,20 @@ struct DecCfg {
   // (three per SM at d = 128, six at d = 64): the other CTAs on the SM hide each one's
   // loads, and K of the next sub-tile loads while this one's softmax and P V run.
   static constexpr int OFF_K = 0, OFF_V = TILE_BYTES;
-  static constexpr int OFF_Q = 2 * TILE_BYTES;  // float q [kDecMaxG][D], scale*log2(e) folded in
+  // q of the heads as the B operand of the score product: bf16 [16 rows][D] (rows past G
+  // zero), D/64 blocks of [16 rows x 128 B], 128-byte swizzle
+  static constexpr int OFF_Q = 2 * TILE_BYTES;
+  static constexpr int Q_BYTES = 16 * D * 2;
   // [4 warps][kDecMaxG][D + 2] float, used only after the last sub-tile has been read and
   // no copy is in flight: it shares the K/V slots
   static constexpr int OFF_RED = 0;
   static_assert(4 * kDecMaxG * (D + 2) * 4 <= 2 * TILE_BYTES, "reduction area");
   // float p [4 warps][32 keys][kDecMaxG]: the probabilities of each warp's keys, read back
   // as broadcasts in P V (one shared load per key instead of one shuffle per head)
-  static constexpr int OFF_P = OFF_Q + kDecMaxG * D * 4;
-  static constexpr int OFF_BAR = OFF_P + 4 * 32 * kDecMaxG * 4;  // k_full, v_full
-  static constexpr int SMEM = OFF_BAR + 2 * 8 + 16;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 4 * 32 * kDecMaxG * 4;  // k_full, v_full, s_done, drain
+  static constexpr int SMEM = OFF_BAR + 4 * 8 + 16;
+  static constexpr uint32_t TM_COLS = 32;  // S^T: 128 lanes (keys) x 16 columns (heads)
 };
 
 struct DecParams {
@@ -73,13 +78,7 @@ struct DecParams {
   int* status;
 };
 
-__device__ __forceinline__ uint4 lds128v(uint32_t addr) {  // ordered after the preceding waits
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ uint2 lds64v(uint32_t addr) {
+__device__ __forceinline__ uint2 lds64v(uint32_t addr) {  // ordered after the preceding waits
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
@@ -129,25 +128,41 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   // while the softmax and P V of s still run; V of s + 1 once P V of s is done
   uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* v_full = k_full + 1;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 2 * 8);
-  float* qs = reinterpret_cast<float*>(smem + C::OFF_Q);
+  uint64_t* s_done = k_full + 2;  // the score product of the current sub-tile is complete
+  uint64_t* drain = k_full + 3;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 4 * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 4 * 8 + 4);
   float* pw = reinterpret_cast<float*>(smem + C::OFF_P) + kw * 32 * HS;  // this warp's [32][HS]
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   if (threadIdx.x == 0) {
     mbar_init(k_full, 1);
     mbar_init(v_full, 1);
+    mbar_init(s_done, 1);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // q of the G heads (heads >= G are zero), scale * log2(e) folded in
-  for (int i = threadIdx.x; i < HG * D; i += NT) {
-    const int hh = i / D, c = i % D;
-    float x = 0.f;
-    if (hh < p.G) x = __bfloat162float(p.q[(static_cast<int64_t>(b) * p.H + g * p.G + hh) * D + c]) * p.scale_log2;
-    qs[i] = x;
+  // q of the heads, bf16, rows past G zero: 16-byte chunk x of row hh
+  for (int i = threadIdx.x; i < 16 * CH; i += NT) {
+    const int hh = i / CH, x = i % CH;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (hh < p.G) v = *reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.H + g * p.G + hh) * D + x * 8);
+    st_shared_v4(sbase + C::OFF_Q + (x >> 3) * (16 * 128) + hh * 128 + (((x & 7) ^ (hh & 7)) << 4), v);
   }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // the score product: A = the K sub-tile (keys x D, K-major), B = q (16 rows x D, K-major)
+  constexpr uint32_t IDESC_S = idesc_bf16(kDecKeys, 16, false);
+  const uint64_t a_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+  const uint64_t b_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
   // K (kind 0) or V (kind 1) of sub-tile s into its slot
   auto issue = [&](int s, int kind) {
     uint8_t* dst = smem + (kind ? C::OFF_V : C::OFF_K);
@@ -177,34 +192,34 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   const int r = kw * 32 + lane;  // this lane's key row within a sub-tile
   int issued_k = min(n_sub, 1), issued_v = issued_k;  // sub-tiles whose K / V loads are issued
   bool failed = false;
+  int mma_issued = 0;  // score products issued (thread 0)
   for (int s = 0; s < n_sub; ++s) {
     const uint32_t par = s & 1;
     if (__syncthreads_or(!mbar_wait(k_full, par, abort_flag))) {  // block-uniform
       failed = true;
       break;
     }
-    const uint32_t kt = sbase + C::OFF_K, vt = sbase + C::OFF_V;
+    const uint32_t vt = sbase + C::OFF_V;
     const int base_key = s * kDecKeys;
-    // ---- scores of the G heads for key r (two partial sums per head)
-    float a0[HS], a1[HS];
+    // ---- scores of the heads for the sub-tile's keys on the tensor core
+    if (threadIdx.x == 0) {
+      tc_fence_after();
 #pragma unroll
-    for (int hh = 0; hh < HS; ++hh) a0[hh] = a1[hh] = 0.f;
-#pragma unroll 4
-    for (int x = 0; x < CH; ++x) {
-      const uint4 kx = lds128v(kt + dec_off(r, x));
-      const float k0f = bf16_lo(kx.x), k1f = bf16_hi(kx.x), k2f = bf16_lo(kx.y), k3f = bf16_hi(kx.y);
-      const float k4f = bf16_lo(kx.z), k5f = bf16_hi(kx.z), k6f = bf16_lo(kx.w), k7f = bf16_hi(kx.w);
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) {
-        const float4 q0 = *reinterpret_cast<const float4*>(qs + (h0 + hh) * D + x * 8);
-        const float4 q1 = *reinterpret_cast<const float4*>(qs + (h0 + hh) * D + x * 8 + 4);
-        ffma2(q0.x, q0.y, k0f, k1f, a0[hh], a1[hh], a0[hh], a1[hh]);
-        ffma2(q0.z, q0.w, k2f, k3f, a0[hh], a1[hh], a0[hh], a1[hh]);
-        ffma2(q1.x, q1.y, k4f, k5f, a0[hh], a1[hh], a0[hh], a1[hh]);
-        ffma2(q1.z, q1.w, k6f, k7f, a0[hh], a1[hh], a0[hh], a1[hh]);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss(tmem, sdesc_add(a_desc, (kk >> 2) * (kDecKeys * 128) + (kk & 3) * 32),
+                    sdesc_add(b_desc, (kk >> 2) * (16 * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
+      mma_commit(s_done);
+      ++mma_issued;
     }
-    // every warp has read K: load the next sub-tile's K
+    if (__syncthreads_or(!mbar_wait(s_done, par, abort_flag))) {
+      failed = true;
+      break;
+    }
+    tc_fence_after();
+    uint32_t sv[16];
+    tmem_ld16(tmem + (static_cast<uint32_t>(kw * 32) << 16), sv);  // lane = key r, column = head
+    tc_fence_before();
+    // every warp has its scores (the product has read K): load the next sub-tile's K
     __syncthreads();
     if (threadIdx.x == 0 && issued_k < n_sub) issue(issued_k, 0);
     ++issued_k;
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     // ---- online softmax per head: warp-wide max, per-lane sums
     float pr[HS], sc[HS], wmax[HS];
 #pragma unroll
-    for (int hh = 0; hh < HS; ++hh) sc[hh] = valid ? a0[hh] + a1[hh] : -INFINITY;
+    for (int hh = 0; hh < HS; ++hh) sc[hh] = valid ? __uint_as_float(sv[h0 + hh]) * p.scale_log2 : -INFINITY;
     if constexpr (HS == 4) {
       // reduce-scatter of the four maxima over lane bits 4 and 3, a butterfly over bits
       // 2..0, then a gather: 10 shuffles instead of 20 (a shuffle issues at a quarter of
@@ -287,12 +302,29 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   if (failed) {
     if (threadIdx.x == 0) {
       record_status(p.status, kStatusTimeout);
-      // let the copies still in flight land before the CTA exits
+      // let the copies and products still in flight land before the CTA exits
       volatile int never = 0;
       if (issued_k > 0 && issued_k <= n_sub) mbar_wait(k_full, (issued_k - 1) & 1, &never);
       if (issued_v > 0 && issued_v <= n_sub) mbar_wait(v_full, (issued_v - 1) & 1, &never);
+      if (mma_issued > 0) {
+        mma_commit(drain);
+        mbar_wait(drain, 0, &never);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TM_COLS);
     }
     return;
+  }
+  // every score product has been read (the s_done waits): TMEM is no longer needed
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
   }
   // ---- merge the four key-quarter warps' states of each head into this split's state
 #pragma unroll
