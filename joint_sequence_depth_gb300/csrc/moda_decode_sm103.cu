@@ -11,10 +11,11 @@
 // K of the next sub-tile loading while P V of this one runs); the extra
 // last split of each (b, g) takes the S depth slots.  Per sub-tile, the scores of the G
 // heads are one tensor-core product S^T = K q^T (M = 128 keys, N = 16 with the heads past
-// G zero, into 16 TMEM columns), read back with lane = key; then lane = d/32 output
-// columns for P V on the CUDA cores (P read back from shared memory as broadcasts).  Each warp keeps, per head, a running max,
-// per-lane denominators and its output numerator; the CTA merges its warps and writes one
-// partial state {max, sum, numerator} per head to a float32 workspace.  A second kernel
+// G zero, into 16 TMEM columns), read back with lane = key; the sub-tile's maximum of
+// each head over all its keys sets the running max; P V is a second product, O^T = V^T
+// P^T (M = 128 channels, N = 16, P^T as bf16 in shared memory), read back with lane =
+// channel and added into the thread's numerators with the heads' rescale factors.  The
+// CTA writes one partial state {max, sum, numerator} per head to a float32 workspace.  A second kernel
 // merges the splits of each (b, h) by the same online rule and divides once.
 //
 // All waits are bounded (sm103_ptx.cuh); a timeout records MODA_ERR_TIMEOUT.
@@ -33,37 +34,35 @@ using namespace sm103;
 constexpr int kDecKeys = 128;    // keys per sub-tile: 4 warps x 32 lanes (per head group)
 constexpr int kDecMaxG = 8;
 
-// Warps of a CTA: four key quarters for each head group.  One head group: splitting the
-// heads over two groups of warps measured slower (both groups read and convert the same
-// K and V rows).
-template <int HG>
-struct DecWarps {
-  static constexpr int NHG = 1;        // head groups
-  static constexpr int HS = HG / NHG;  // heads per group
-  static constexpr int THREADS = 128 * NHG;
-};
+// Threads of a CTA: 128, thread t = TMEM lane t (key t of a sub-tile for the scores,
+// channel t for P V).
+constexpr int kDecThreads = 128;
 
 template <int D>
 struct DecCfg {
   static constexpr int TILE_BYTES = kDecKeys * D * 2;  // one K (or V) sub-tile, bf16
-  // One K slot and one V slot, each with a barrier of its own, and many resident CTAs
+  // One V slot and one K slot, each with a barrier of its own, and many resident CTAs
   // (three per SM at d = 128, six at d = 64): the other CTAs on the SM hide each one's
-  // loads, and K of the next sub-tile loads while this one's softmax and P V run.
-  static constexpr int OFF_K = 0, OFF_V = TILE_BYTES;
+  // loads, and K of the next sub-tile loads while this one's softmax and P V run.  V
+  // comes first: at d = 64 the P V product reads 128 rows of V^T, the last 64 of which
+  // (from the K slot behind it) give output lanes that are never used.
+  static constexpr int OFF_V = 0, OFF_K = TILE_BYTES;
   // q of the heads as the B operand of the score product: bf16 [16 rows][D] (rows past G
   // zero), D/64 blocks of [16 rows x 128 B], 128-byte swizzle
   static constexpr int OFF_Q = 2 * TILE_BYTES;
   static constexpr int Q_BYTES = 16 * D * 2;
-  // [4 warps][kDecMaxG][D + 2] float, used only after the last sub-tile has been read and
-  // no copy is in flight: it shares the K/V slots
-  static constexpr int OFF_RED = 0;
-  static_assert(4 * kDecMaxG * (D + 2) * 4 <= 2 * TILE_BYTES, "reduction area");
-  // float p [4 warps][32 keys][kDecMaxG]: the probabilities of each warp's keys, read back
-  // as broadcasts in P V (one shared load per key instead of one shuffle per head)
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 4 * 32 * kDecMaxG * 4;  // k_full, v_full, s_done, drain
-  static constexpr int SMEM = OFF_BAR + 4 * 8 + 16;
-  static constexpr uint32_t TM_COLS = 32;  // S^T: 128 lanes (keys) x 16 columns (heads)
+  // P^T of a sub-tile as the B operand of P V: bf16 [16 rows (heads)][128 keys], keys
+  // [0, 64) then [64, 128) as two blocks of [16 rows x 128 B], 128-byte swizzle
+  static constexpr int OFF_PT = OFF_Q + Q_BYTES;
+  static constexpr int PT_BYTES = 16 * kDecKeys * 2;
+  // per-warp maxima of a sub-tile, float [4 warps][kDecMaxG]; per-warp denominators at
+  // the end
+  static constexpr int OFF_WM = OFF_PT + PT_BYTES;
+  static constexpr int OFF_BAR = OFF_WM + 4 * kDecMaxG * 4;  // k_full, v_full, s_done, pv_done, drain
+  static constexpr int SMEM = OFF_BAR + 5 * 8 + 16;
+  // TMEM: S^T [0, 16) (lane = key, column = head), the sub-tile's P V [16, 32) (lane =
+  // channel, column = head)
+  static constexpr uint32_t TM_COLS = 32, TM_S = 0, TM_PV = 16;
 };
 
 struct DecParams {
@@ -78,33 +77,13 @@ struct DecParams {
   int* status;
 };
 
-__device__ __forceinline__ uint2 lds64v(uint32_t addr) {  // ordered after the preceding waits
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32v(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-// Byte offset of 16-byte chunk x of row r in a [kDecKeys x D] bf16 tile stored as D/64
-// blocks of [kDecKeys x 128 B], 128-byte swizzled (the layout TMA writes).
-__device__ __forceinline__ uint32_t dec_off(int r, int x) {
-  return static_cast<uint32_t>((x >> 3) * (kDecKeys * 128) + r * 128 + (((x & 7) ^ (r & 7)) << 4));
-}
-
 template <int D, int HG>
-__global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
+__global__ void __launch_bounds__(kDecThreads, 1)
     moda_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmKd, const __grid_constant__ CUtensorMap tmVd,
                        const DecParams p) {
   using C = DecCfg<D>;
-  constexpr int CH = D / 8;    // 16-byte chunks per row
-  constexpr int CPL = D / 32;  // output columns per lane
-  constexpr int HS = DecWarps<HG>::HS;
-  constexpr int NT = DecWarps<HG>::THREADS;
+  constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
@@ -112,7 +91,7 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kw = warp & 3, h0 = (warp >> 2) * HS;  // key quarter, first head of this warp
+  const int r = threadIdx.x;  // key of a sub-tile (scores), channel (P V)
   const int split = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const bool depth = split == p.n_seq;
@@ -124,32 +103,36 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   const CUtensorMap* mv = depth ? &tmVd : &tmV;
   const int row0 = depth ? bg * p.S : static_cast<int>(bg * p.cap) + k0;  // host checks the int range
 
-  // K of sub-tile s + 1 is loaded as soon as every warp has its scores for sub-tile s,
-  // while the softmax and P V of s still run; V of s + 1 once P V of s is done
+  // K of sub-tile s + 1 is loaded once the score product of sub-tile s has read K, while
+  // the softmax and P V of s still run; V of s + 1 once the P V product of s has read V
   uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* v_full = k_full + 1;
-  uint64_t* s_done = k_full + 2;  // the score product of the current sub-tile is complete
-  uint64_t* drain = k_full + 3;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 4 * 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 4 * 8 + 4);
-  float* pw = reinterpret_cast<float*>(smem + C::OFF_P) + kw * 32 * HS;  // this warp's [32][HS]
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  uint64_t* s_done = k_full + 2;   // the score product of the current sub-tile is complete
+  uint64_t* pv_done = k_full + 3;  // its P V product is complete
+  uint64_t* drain = k_full + 4;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 5 * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 5 * 8 + 4);
+  float* wm = reinterpret_cast<float*>(smem + C::OFF_WM);  // [4][kDecMaxG]
 
   if (threadIdx.x == 0) {
     mbar_init(k_full, 1);
     mbar_init(v_full, 1);
     mbar_init(s_done, 1);
+    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   // q of the heads, bf16, rows past G zero: 16-byte chunk x of row hh
-  for (int i = threadIdx.x; i < 16 * CH; i += NT) {
+  for (int i = threadIdx.x; i < 16 * CH; i += kDecThreads) {
     const int hh = i / CH, x = i % CH;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (hh < p.G) v = *reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(b) * p.H + g * p.G + hh) * D + x * 8);
     st_shared_v4(sbase + C::OFF_Q + (x >> 3) * (16 * 128) + hh * 128 + (((x & 7) ^ (hh & 7)) << 4), v);
   }
+  // P^T rows of heads past G stay zero
+  for (int i = threadIdx.x; i < C::PT_BYTES / 16; i += kDecThreads)
+    st_shared_v4(sbase + C::OFF_PT + i * 16, make_uint4(0, 0, 0, 0));
   fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(tmem_slot, C::TM_COLS);
@@ -159,10 +142,17 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_tm = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
   // the score product: A = the K sub-tile (keys x D, K-major), B = q (16 rows x D, K-major)
   constexpr uint32_t IDESC_S = idesc_bf16(kDecKeys, 16, false);
-  const uint64_t a_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-  const uint64_t b_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+  const uint64_t k_desc = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+  const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+  // the P V product (O^T = V^T P^T): A = V^T (128 channels x keys, channels contiguous,
+  // 64-channel blocks 16 KB apart), B = P^T (16 rows x keys, K-major)
+  constexpr uint32_t IDESC_PV = idesc_bf16(128, 16, false) | (1u << 15);  // A M-major
+  const uint64_t v_desc = sdesc_sw128(sbase + C::OFF_V, kDecKeys * 128, 1024);
+  const uint64_t pt_desc = sdesc_sw128(sbase + C::OFF_PT, 16, 1024);
+
   // K (kind 0) or V (kind 1) of sub-tile s into its slot
   auto issue = [&](int s, int kind) {
     uint8_t* dst = smem + (kind ? C::OFF_V : C::OFF_K);
@@ -181,33 +171,32 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     }
   }
 
-  float m[HS], l[HS], o[HS][CPL];
+  // The split's state per head: the running max (the same in every thread), this thread's
+  // part of the denominator (over its keys) and, for channel r, the numerator.
+  float m[HG], l[HG], o[HG];
 #pragma unroll
-  for (int hh = 0; hh < HS; ++hh) {
+  for (int hh = 0; hh < HG; ++hh) {
     m[hh] = -INFINITY;
     l[hh] = 0.f;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) o[hh][c] = 0.f;
+    o[hh] = 0.f;
   }
-  const int r = kw * 32 + lane;  // this lane's key row within a sub-tile
   int issued_k = min(n_sub, 1), issued_v = issued_k;  // sub-tiles whose K / V loads are issued
+  int mma_issued = 0;                                  // products issued (thread 0)
   bool failed = false;
-  int mma_issued = 0;  // score products issued (thread 0)
   for (int s = 0; s < n_sub; ++s) {
     const uint32_t par = s & 1;
     if (__syncthreads_or(!mbar_wait(k_full, par, abort_flag))) {  // block-uniform
       failed = true;
       break;
     }
-    const uint32_t vt = sbase + C::OFF_V;
     const int base_key = s * kDecKeys;
     // ---- scores of the heads for the sub-tile's keys on the tensor core
     if (threadIdx.x == 0) {
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16_ss(tmem, sdesc_add(a_desc, (kk >> 2) * (kDecKeys * 128) + (kk & 3) * 32),
-                    sdesc_add(b_desc, (kk >> 2) * (16 * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
+        mma_bf16_ss(tmem + C::TM_S, sdesc_add(k_desc, (kk >> 2) * (kDecKeys * 128) + (kk & 3) * 32),
+                    sdesc_add(q_desc, (kk >> 2) * (16 * 128) + (kk & 3) * 32), IDESC_S, kk > 0);
       mma_commit(s_done);
       ++mma_issued;
     }
@@ -217,148 +206,112 @@ __global__ void __launch_bounds__(DecWarps<HG>::THREADS, 1)
     }
     tc_fence_after();
     uint32_t sv[16];
-    tmem_ld16(tmem + (static_cast<uint32_t>(kw * 32) << 16), sv);  // lane = key r, column = head
+    tmem_ld16(lane_tm + C::TM_S, sv);  // lane = key r, column = head
     tc_fence_before();
-    // every warp has its scores (the product has read K): load the next sub-tile's K
-    __syncthreads();
+    // the product has read K: load the next sub-tile's K
     if (threadIdx.x == 0 && issued_k < n_sub) issue(issued_k, 0);
     ++issued_k;
     const bool valid = base_key + r < n_keys;
-    // ---- online softmax per head: warp-wide max, per-lane sums
-    float pr[HS], sc[HS], wmax[HS];
+    float sc[HG];
 #pragma unroll
-    for (int hh = 0; hh < HS; ++hh) sc[hh] = valid ? __uint_as_float(sv[h0 + hh]) * p.scale_log2 : -INFINITY;
-    if constexpr (HS == 4) {
-      // reduce-scatter of the four maxima over lane bits 4 and 3, a butterfly over bits
-      // 2..0, then a gather: 10 shuffles instead of 20 (a shuffle issues at a quarter of
-      // the FMA rate)
-      const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-      float y[2];
+    for (int hh = 0; hh < HG; ++hh) {
+      sc[hh] = valid ? __uint_as_float(sv[hh]) * p.scale_log2 : -INFINITY;
+      float w = sc[hh];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-        y[u] = fmaxf(b4 ? sc[u + 2] : sc[u], __shfl_xor_sync(0xffffffffu, b4 ? sc[u] : sc[u + 2], 16));
-      float z = fmaxf(b3 ? y[1] : y[0], __shfl_xor_sync(0xffffffffu, b3 ? y[0] : y[1], 8));
-#pragma unroll
-      for (int off = 4; off >= 1; off >>= 1) z = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, off));
-#pragma unroll
-      for (int hh = 0; hh < 4; ++hh) wmax[hh] = __shfl_sync(0xffffffffu, z, hh * 8);  // lane of head hh
-    } else {
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) {
-        float wm = sc[hh];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
-        wmax[hh] = wm;
-      }
+      for (int off = 16; off >= 1; off >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, off));
+      if (lane == 0) wm[warp * kDecMaxG + hh] = w;
     }
+    __syncthreads();
+    // ---- online softmax with the sub-tile's maximum over all four warps
+    float corr[HG];
 #pragma unroll
-    for (int hh = 0; hh < HS; ++hh) {
-      const float m_new = fmaxf(m[hh], wmax[hh]);
-      const float corr = (m[hh] == -INFINITY) ? 0.f : ex2(m[hh] - m_new);
-      pr[hh] = valid ? ex2(sc[hh] - m_new) : 0.f;
-      l[hh] = l[hh] * corr + pr[hh];
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) o[hh][c] *= corr;
+    for (int hh = 0; hh < HG; ++hh) {
+      const float cmax = fmaxf(fmaxf(wm[hh], wm[kDecMaxG + hh]), fmaxf(wm[2 * kDecMaxG + hh], wm[3 * kDecMaxG + hh]));
+      const float m_new = fmaxf(m[hh], cmax);
+      corr[hh] = (m[hh] == -INFINITY) ? 0.f : ex2(m[hh] - m_new);
+      const float pr = valid ? ex2(sc[hh] - m_new) : 0.f;
+      l[hh] = l[hh] * corr[hh] + pr;
       m[hh] = m_new;
+      // P^T[hh][r] (bf16) for the P V product
+      const __nv_bfloat16 pb = __float2bfloat16_rn(pr);
+      const uint32_t addr = sbase + C::OFF_PT + (r >> 6) * (16 * 128) + hh * 128 +
+                            ((((r & 63) >> 3) ^ (hh & 7)) << 4) + (r & 7) * 2;
+      asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&pb))
+                   : "memory");
     }
     if (__syncthreads_or(!mbar_wait(v_full, par, abort_flag))) {
       failed = true;
       break;
     }
-    // this lane's probabilities for the warp's P V loop (the previous sub-tile's loop has
-    // read its values before the barriers above)
+    if (!valid) {
+      // rows past the keys read (a cache's positions past T, a ring's unread slots) may
+      // hold anything, NaN included: they enter the product with P = 0, so make them zero
 #pragma unroll
-    for (int hh = 0; hh < HS; ++hh) pw[lane * HS + hh] = pr[hh];
-    __syncwarp();
-    // ---- P V over this warp's valid keys; lane owns columns [lane*CPL, lane*CPL + CPL)
-    const int n_here = min(32, n_keys - base_key - kw * 32);  // warp-uniform
-    const int xc = (lane * CPL) >> 3, sub = ((lane * CPL) & 7) * 2;
-    for (int j = 0; j < n_here; ++j) {
-      const int rv = kw * 32 + j;
-      float vf[CPL];
-      if constexpr (CPL == 4) {
-        const uint2 vw = lds64v(vt + dec_off(rv, xc) + sub);
-        vf[0] = bf16_lo(vw.x);
-        vf[1] = bf16_hi(vw.x);
-        vf[2] = bf16_lo(vw.y);
-        vf[3] = bf16_hi(vw.y);
-      } else {
-        const uint32_t vw = lds32v(vt + dec_off(rv, xc) + sub);
-        vf[0] = bf16_lo(vw);
-        vf[1] = bf16_hi(vw);
-      }
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) {
-        const float pj = pw[j * HS + hh];
-#pragma unroll
-        for (int c = 0; c < CPL; c += 2) ffma2(pj, pj, vf[c], vf[c + 1], o[hh][c], o[hh][c + 1], o[hh][c], o[hh][c + 1]);
-      }
+      for (int x = 0; x < CH; ++x)
+        st_shared_v4(sbase + C::OFF_V + (x >> 3) * (kDecKeys * 128) + r * 128 + ((x & 7) << 4), make_uint4(0, 0, 0, 0));
     }
-    // every warp has read V: load the next sub-tile's V
+    fence_proxy_async_smem();
     __syncthreads();
+    // ---- P V on the tensor core: O^T of the sub-tile (lane = channel, column = head)
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kDecKeys / 16; ++kk)
+        mma_bf16_ss(tmem + C::TM_PV, sdesc_add(v_desc, kk * 2048),
+                    sdesc_add(pt_desc, (kk >> 2) * (16 * 128) + (kk & 3) * 32), IDESC_PV, kk > 0);
+      mma_commit(pv_done);
+      ++mma_issued;
+    }
+    if (__syncthreads_or(!mbar_wait(pv_done, par, abort_flag))) {
+      failed = true;
+      break;
+    }
+    tc_fence_after();
+    uint32_t pv[16];
+    tmem_ld16(lane_tm + C::TM_PV, pv);
+    tc_fence_before();
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) o[hh] = o[hh] * corr[hh] + __uint_as_float(pv[hh]);
+    // the product has read V and P^T: load the next sub-tile's V
     if (threadIdx.x == 0 && issued_v < n_sub) issue(issued_v, 1);
     ++issued_v;
   }
-  if (failed) {
-    if (threadIdx.x == 0) {
-      record_status(p.status, kStatusTimeout);
-      // let the copies and products still in flight land before the CTA exits
-      volatile int never = 0;
-      if (issued_k > 0 && issued_k <= n_sub) mbar_wait(k_full, (issued_k - 1) & 1, &never);
-      if (issued_v > 0 && issued_v <= n_sub) mbar_wait(v_full, (issued_v - 1) & 1, &never);
-      if (mma_issued > 0) {
-        mma_commit(drain);
-        mbar_wait(drain, 0, &never);
-      }
+  if (failed && threadIdx.x == 0) {
+    record_status(p.status, kStatusTimeout);
+    // let the copies and products still in flight land before the CTA exits
+    volatile int never = 0;
+    if (issued_k > 0 && issued_k <= n_sub) mbar_wait(k_full, (issued_k - 1) & 1, &never);
+    if (issued_v > 0 && issued_v <= n_sub) mbar_wait(v_full, (issued_v - 1) & 1, &never);
+    if (mma_issued > 0) {
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never);
     }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(tmem, C::TM_COLS);
-    }
-    return;
   }
-  // every score product has been read (the s_done waits): TMEM is no longer needed
+  // every product has been read (the waits above): TMEM is no longer needed
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }
-  // ---- merge the four key-quarter warps' states of each head into this split's state
+  if (failed) return;
+  // ---- this split's state: {max, denominator, numerator[D]} per head
 #pragma unroll
-  for (int hh = 0; hh < HS; ++hh) {
+  for (int hh = 0; hh < HG; ++hh) {
     float ls = l[hh];
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-    float* w = red + (kw * kDecMaxG + h0 + hh) * (D + 2);
-    if (lane == 0) {
-      w[0] = m[hh];
-      w[1] = ls;
-    }
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) w[2 + lane * CPL + c] = o[hh][c];
+    if (lane == 0) wm[warp * kDecMaxG + hh] = ls;
   }
   __syncthreads();
   const int64_t row_base = static_cast<int64_t>(split) * p.B * p.H + static_cast<int64_t>(b) * p.H + g * p.G;
-  for (int i = threadIdx.x; i < p.G * (D + 2); i += NT) {
-    const int hh = i / (D + 2), e = i % (D + 2);
-    float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red[(w * kDecMaxG + hh) * (D + 2)]);
-    float val;
-    if (e == 0) {
-      val = mx;
-    } else {
-      val = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = red[(w * kDecMaxG + hh) * (D + 2)];
-        if (mw != -INFINITY) val += red[(w * kDecMaxG + hh) * (D + 2) + e] * ex2(mw - mx);
-      }
+  for (int hh = 0; hh < p.G && hh < HG; ++hh) {
+    float* dst = p.part + (row_base + hh) * (D + 2);
+    if (r < D) dst[2 + r] = o[hh];
+    if (r == 0) {
+      dst[0] = m[hh];
+      dst[1] = wm[hh] + wm[kDecMaxG + hh] + wm[2 * kDecMaxG + hh] + wm[3 * kDecMaxG + hh];
     }
-    p.part[(row_base + hh) * (D + 2) + e] = val;
   }
 }
 
@@ -455,7 +408,7 @@ cudaError_t launch_dec(const DecodeArgs& a, const DecodeSplit& sp, cudaStream_t 
   cudaError_t e = ensure_dynamic_smem(moda_decode_kernel<D, HG>, C::SMEM, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(sp.n_split), static_cast<unsigned>(groups));
-  moda_decode_kernel<D, HG><<<grid, DecWarps<HG>::THREADS, C::SMEM, s>>>(tk, tv, tkd, tvd, p);
+  moda_decode_kernel<D, HG><<<grid, kDecThreads, C::SMEM, s>>>(tk, tv, tkd, tvd, p);
   DecMergeParams m;
   m.BH = pr.B * pr.H;
   m.n_split = sp.n_split;
