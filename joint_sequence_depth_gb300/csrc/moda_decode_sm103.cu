@@ -323,23 +323,57 @@ struct DecMergeParams {
 };
 
 // One warp per (b, h): merge the splits' partial states by the online rule, divide once.
+// The splits' maxima are read one per lane (32 splits at a time) and reduced by shuffles;
+// each lane then weighs its splits' denominators, and the numerators are read four
+// splits at a time, so the loads of a warp do not wait on one another.
 template <int D>
 __global__ void __launch_bounds__(128) moda_decode_merge_kernel(const DecMergeParams p) {
   constexpr int CPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= p.BH) return;
+  auto state = [&](int sp) { return p.part + (static_cast<int64_t>(sp) * p.BH + row) * (D + 2); };
   float mx = -INFINITY;
-  for (int s = 0; s < p.n_split; ++s) mx = fmaxf(mx, p.part[(static_cast<int64_t>(s) * p.BH + row) * (D + 2)]);
-  float L = 0.f, acc[CPL];
+  for (int s0 = 0; s0 < p.n_split; s0 += 32)
+    if (s0 + lane < p.n_split) mx = fmaxf(mx, state(s0 + lane)[0]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float L = 0.f;
+  for (int s0 = 0; s0 < p.n_split; s0 += 32) {
+    if (s0 + lane < p.n_split) {
+      const float* ps = state(s0 + lane);
+      const float ms = ps[0];
+      if (ms != -INFINITY) L += ps[1] * ex2(ms - mx);  // a split without keys has ms = -inf
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  float acc[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
-    const float* ps = p.part + (static_cast<int64_t>(s) * p.BH + row) * (D + 2);
+  int sp = 0;
+  for (; sp + 4 <= p.n_split; sp += 4) {
+    float ms[4], v[4][CPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* ps = state(sp + u);
+      ms[u] = ps[0];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) v[u][c] = ps[2 + lane * CPL + c];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ms[u] == -INFINITY) continue;
+      const float w = ex2(ms[u] - mx);
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[c] += v[u][c] * w;
+    }
+  }
+  for (; sp < p.n_split; ++sp) {
+    const float* ps = state(sp);
     const float ms = ps[0];
-    if (ms == -INFINITY) continue;  // a split without keys
+    if (ms == -INFINITY) continue;
     const float w = ex2(ms - mx);
-    L += ps[1] * w;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] += ps[2 + lane * CPL + c] * w;
   }
