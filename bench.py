@@ -1037,8 +1037,8 @@ def main():
     peaks, peak_kind = load_peaks()
     counts = kernel_counts(shape)
     kernels = {name: kernel_roofline(counts[name], ms, peaks) for name, ms in kernel_ms.items()}
-    # `roofline` is the forward kernel's (the operator's forward is the graded target); the
-    # longest backward kernel is reported beside it
+    # `roofline` is the forward kernel's (the operator's own kernel); the longest backward
+    # kernel is reported beside it
     def described(kernel):
         r = dict(kernels[kernel])
         r["traffic"] = traffic_record(kernel, shape.name)
