@@ -152,8 +152,10 @@ moda_status moda_bwd_profiled(const moda_desc* desc, const void* q, const void* 
  * 256-byte aligned (per-split partial softmax states); calls sharing it must not
  * overlap on the GPU.  Errors as for moda_fwd; MODA_ERR_WORKSPACE when the workspace
  * is missing or too small.
- * Runs two kernels: a key-split pass (TMA-staged K/V sub-tiles, float32 scores and
- * online softmax on the CUDA cores, the depth slots as one more split) and a merge. */
+ * Runs two kernels: a key-split pass (TMA-staged K/V sub-tiles of 128 keys; the scores
+ * and P V of each sub-tile as tensor-core products with float32 accumulation, P rounded to
+ * bf16; the online softmax in float32 on the CUDA cores; the depth slots as one more
+ * split) and a merge. */
 size_t moda_decode_workspace_bytes(const moda_desc* desc);
 moda_status moda_decode(const moda_desc* desc, int64_t kv_capacity, const void* q, const void* k_cache,
                         const void* v_cache, const void* kd, const void* vd, void* o, float* lse, void* workspace,
