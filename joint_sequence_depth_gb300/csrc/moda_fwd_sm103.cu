@@ -180,13 +180,16 @@ __device__ __forceinline__ Unit unit_at(const FwdTcParams& p, int c, int k) {
 
 // K/V items of a unit, in the order the loader issues them (with per = n_ch * tw items of
 // one kind per depth step, tw = 2 query tiles or 1 when tile 1 is empty):
-//   depth step i:   K of chunk c of tile t at 2 i per + c tw + t (the two tiles' chunks
-//                   alternate), then V likewise at + per;
+//   depth step i:   the K items of the step's chunks, then their V items at + per.  With
+//                   one MMA issuer per query tile (d = 64) the two tiles' chunks
+//                   alternate (chunk c of tile t at 2 i per + c tw + t); the single issuer
+//                   (d = 128) takes tile 0's chunks, then tile 1's (2 i per + t n_ch + c),
+//                   so that tile 0's softmax starts while tile 1's products are issued;
 //   sequence steps: K_j, V_j, each shared by both query tiles.
-// With one MMA issuer per query tile (d = 64: S of the next step issued before the P V of
-// this one) the sequence's K_0 is hoisted between the K and the V items of the last depth
-// step ("hoist"); the single issuer (d = 128) takes both tiles' depth P V before S of the
-// next step, and K_0 stays in its place.
+// With one issuer per tile (S of the next step issued before the P V of this one) the
+// sequence's K_0 is hoisted between the K and the V items of the last depth step
+// ("hoist"); the single issuer takes both tiles' depth P V before S of the next step, and
+// K_0 stays in its place.
 // Every consumer takes its items in load order, and an issuer's consecutive items are at
 // most two apart within a unit (a unit's first item is waited for after its Q tile, which
 // the loader issues after every item of the previous unit).  So when an issuer waits for
@@ -194,13 +197,15 @@ __device__ __forceinline__ Unit unit_at(const FwdTcParams& p, int c, int k) {
 // was released: the earlier use of x's full barrier (even and odd loads of a slot have a
 // barrier each) has completed, and the parity wait cannot pass on it.
 struct Items {
-  int base, tw, per, n_d, hoist, nd;  // nd: items of the depth steps (with a hoisted K_0)
+  int base, tw, per, n_ch, n_d, hoist, nd;  // nd: items of the depth steps (with a hoisted K_0)
+  bool tile_major;                          // the single issuer's order of a step's chunks
   __device__ __forceinline__ Items(const FwdTcParams& p, const Unit& u, int b, bool split)
-      : base(b), tw(u.nt[1] > 0 ? 2 : 1), per(p.n_ch * tw), n_d(p.n_d), hoist(split && p.n_d > 0 ? 1 : 0),
-        nd(p.n_d > 0 ? 2 * p.n_d * per + hoist : 0) {}
-  __device__ __forceinline__ int dk(int i, int c, int t) const { return base + 2 * i * per + c * tw + t; }
+      : base(b), tw(u.nt[1] > 0 ? 2 : 1), per(p.n_ch * tw), n_ch(p.n_ch), n_d(p.n_d),
+        hoist(split && p.n_d > 0 ? 1 : 0), nd(p.n_d > 0 ? 2 * p.n_d * per + hoist : 0), tile_major(!split) {}
+  __device__ __forceinline__ int chunk_off(int c, int t) const { return tile_major ? t * n_ch + c : c * tw + t; }
+  __device__ __forceinline__ int dk(int i, int c, int t) const { return base + 2 * i * per + chunk_off(c, t); }
   __device__ __forceinline__ int dv(int i, int c, int t) const {
-    return base + 2 * i * per + per + (i == n_d - 1 ? hoist : 0) + c * tw + t;
+    return base + 2 * i * per + per + (i == n_d - 1 ? hoist : 0) + chunk_off(c, t);
   }
   __device__ __forceinline__ int sk(int j) const {
     return hoist ? (j == 0 ? base + 2 * (n_d - 1) * per + per : base + nd + 2 * j - 1) : base + nd + 2 * j;
@@ -221,8 +226,8 @@ struct Items {
       }
       kind = rem < per ? 0 : 1;
       const int e = rem < per ? rem : rem - per - lastd;
-      c = e / tw;
-      t = e % tw;
+      c = tile_major ? e % n_ch : e / tw;
+      t = tile_major ? e / n_ch : e % tw;
     } else {
       const int q = r - nd + hoist;  // index in K_0 V_0 K_1 V_1 ...
       j = q >> 1;
@@ -464,65 +469,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (!two) mma_commit_warp(&q_empty[1]);  // tile 1 unused in this unit
         const Items it(p, u, base, false);
-        const int tw = two ? 2 : 1;
-        // S of depth step i: chunk by chunk, each tile's product into its S, masked to the
-        // chunk's rows, then a commit per tile
-        auto depth_s = [&](int i) -> bool {
+        // S of depth step i of tile t: every chunk's product into S_t, masked to the
+        // chunk's rows, then one commit
+        auto depth_s = [&](int t, int i) -> bool {
+          const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
           for (int c = 0; c < p.n_ch; ++c) {
+            const int item = it.dk(i, c, t);
+            if (!wait_item(item)) return false;
+            tc_fence_after();
             uint32_t mask[4];
             rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
-            for (int t = 0; t < tw; ++t) {
-              const int item = it.dk(i, c, t);
-              if (!wait_item(item)) return false;
-              tc_fence_after();
-              const uint64_t q_desc = sdesc_add(q_desc0, t * C::TILE_BYTES);
-              const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
-              if (elect_one()) {
+            const uint64_t k_desc = sdesc_add(kv_desc_k, (item % C::NSLOT) * C::TILE_BYTES);
+            if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                  mma_bf16_ss_mask(tmem + C::tm_s(t), sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
-                                   sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), idesc_d, kk > 0, mask);
-              }
-              __syncwarp();
-              release(item);
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_bf16_ss_mask(tmem + C::tm_s(t), sdesc_add(q_desc, (kk >> 2) * (BM * 128) + (kk & 3) * 32),
+                                 sdesc_add(k_desc, (kk >> 2) * (BN * 128) + (kk & 3) * 32), idesc_d, kk > 0, mask);
             }
+            __syncwarp();
+            release(item);
           }
-          for (int t = 0; t < tw; ++t) mma_commit_warp(&s_full[t]);
+          mma_commit_warp(&s_full[t]);
           return true;
         };
-        // O_t += P_t V of depth step i once both tiles' P are written: chunk by chunk, each
-        // product masked to the chunk's rows (step 0 starts each row's O)
-        auto depth_pv = [&](int i) -> bool {
-          for (int t = 0; t < tw; ++t) {
-            uint32_t& pc = t ? pcnt1 : pcnt0;
-            if (!warp_wait(&p_full[t], pc & 1, abort_flag) ||
-                (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag)))
-              return false;
-            ++pc;
-          }
+        // O_t += P_t V of depth step i once P_t is written: each chunk's product masked to
+        // the chunk's rows (step 0 starts each row's O)
+        auto depth_pv = [&](int t, int i) -> bool {
+          uint32_t& pc = t ? pcnt1 : pcnt0;
+          if (!warp_wait(&p_full[t], pc & 1, abort_flag) ||
+              (i == 0 && k > 0 && !warp_wait(&o_free[t], (k - 1) & 1, abort_flag)))
+            return false;
+          ++pc;
           tc_fence_after();
           for (int c = 0; c < p.n_ch; ++c) {
+            const int item = it.dv(i, c, t);
+            if (!wait_item(item)) return false;
+            tc_fence_after();
             uint32_t mask[4];
             rows_mask(c * p.dpt * p.G, min((c + 1) * p.dpt, p.P) * p.G, mask);
-            for (int t = 0; t < tw; ++t) {
-              const int item = it.dv(i, c, t);
-              if (!wait_item(item)) return false;
-              tc_fence_after();
-              const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
-              if (elect_one()) {
-                for (int kk = 0; kk < p.nd_keys / 16; ++kk)
-                  mma_bf16_ts_mask(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, sdesc_add(v_desc, kk * 16 * 128),
-                                   IDESC_O, (i > 0 || kk > 0) ? 1u : 0u, mask);
-              }
-              __syncwarp();
-              release(item);
+            const uint64_t v_desc = sdesc_add(kv_desc_v, (item % C::NSLOT) * C::TILE_BYTES);
+            if (elect_one()) {
+              for (int kk = 0; kk < p.nd_keys / 16; ++kk)
+                mma_bf16_ts_mask(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, sdesc_add(v_desc, kk * 16 * 128),
+                                 IDESC_O, (i > 0 || kk > 0) ? 1u : 0u, mask);
             }
+            __syncwarp();
+            release(item);
           }
           return true;
         };
         // S of step 0
         if (p.n_d > 0) {
-          if (!depth_s(0)) {
+          if (!depth_s(0, 0) || (two && !depth_s(1, 0))) {
             ok = false;
             break;
           }
@@ -540,16 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           release(it.sk(0));
         }
-        // ---- depth steps: each query tile has K and V items of its own.  Both tiles' P V
-        // first, then S of step i+1 (the next depth step, or the first sequence step,
+        // ---- depth steps: each query tile has K and V items of its own.  Tile 0's P V,
+        // tile 1's, then S of step i+1 (the next depth step, or the first sequence step,
         // whose K both tiles read): the items are consumed in the order they are loaded.
         for (int i = 0; ok && i < p.n_d; ++i) {
-          if (!depth_pv(i)) {
+          if (!depth_pv(0, i) || (two && !depth_pv(1, i))) {
             ok = false;
             break;
           }
           if (i + 1 < p.n_d) {
-            if (!depth_s(i + 1)) {
+            if (!depth_s(0, i + 1) || (two && !depth_s(1, i + 1))) {
               ok = false;
               break;
             }
