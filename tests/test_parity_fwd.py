@@ -43,6 +43,8 @@ SMALL = [
     # more than 128 slots read: the depth keys take two depth steps of one position each
     ("bf16_d64_g4_slots_gt_tile", 1, 8, 2, 200, 64, 160, bf16),
     ("bf16_d128_g2_slots_gt_tile", 1, 4, 2, 150, 128, 130, bf16),
+    # G = 1 and 160 slots: 128 one-position chunks per depth step, two depth steps
+    ("bf16_d64_g1_slots_gt_tile", 1, 2, 2, 150, 64, 160, bf16),
     # G = 3: 126 of a tile's 128 rows in use, depth chunks of 5 positions (15 rows)
     ("bf16_d64_g3_s24", 1, 6, 2, 300, 64, 24, bf16),
 ]

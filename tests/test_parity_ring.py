@@ -149,6 +149,29 @@ def test_ring_decode(case):
     assert max_abs(as_f64(lse), rl) < TOL_OUT[bf16], max_abs(as_f64(lse), rl)
 
 
+@pytest.mark.parametrize("case", [c for c in NAN_CASES if c[-1] == bf16], ids=[c[0] for c in NAN_CASES if c[-1] == bf16])
+def test_decode_unread_slots_holding_nan_and_inf_change_nothing(case):
+    """The decode step reads only slots 0 .. S-1 of the newest position's ring; the others,
+    NaN (keys) and +/-Inf (values), enter no product (0 * NaN would poison one)."""
+    name, B, H, Hkv, T, d, C, S, dt = case
+    shape = Shape(name, B, H, Hkv, T, d, S, dt)
+    x = make_inputs(shape, seed=zlib.crc32(name.encode()) % 1000 + 81)
+    ring_k = torch.full((B, Hkv, C, d), float("nan"), dtype=dt)
+    ring_v = torch.full((B, Hkv, C, d), float("inf"), dtype=dt)
+    ring_v[..., ::2] = float("-inf")
+    ring_k[:, :, :S] = x["kd"][:, :, T - 1]
+    ring_v[:, :, :S] = x["vd"][:, :, T - 1]
+    q_new = x["q"][:, :, T - 1].contiguous()
+    o, lse = binding.moda_decode(q_new.cuda(), x["k"].cuda(), x["v"].cuda(), ring_k.cuda(), ring_v.cuda(), slots=S)
+    torch.cuda.synchronize()
+    assert binding.moda_device_status() == 0
+    ro, rl = oracle.decode(as_f64(q_new), as_f64(x["k"]), as_f64(x["v"]), as_f64(x["kd"][:, :, T - 1]),
+                           as_f64(x["vd"][:, :, T - 1]))
+    assert np.isfinite(as_f64(o)).all() and np.isfinite(as_f64(lse)).all()
+    assert max_abs(as_f64(o), ro) < TOL_OUT[dt], max_abs(as_f64(o), ro)
+    assert max_abs(as_f64(lse), rl) < TOL_OUT[dt], max_abs(as_f64(lse), rl)
+
+
 def test_ring_rejects_capacity_below_slots():
     """slot_capacity below S is an argument error (nothing launched)."""
     q = torch.zeros(1, 2, 8, 64, dtype=bf16, device="cuda")
